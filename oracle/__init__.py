@@ -1,0 +1,7 @@
+"""fp64 CPU oracle of the fused chunked KL loss.
+
+Test infrastructure: only the tests, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may use it; the CUDA library never does.
+"""
+
+from .kl_oracle import dense_teacher, fwd_bwd, student_lse, teacher_log_probs  # noqa: F401

@@ -1,0 +1,21 @@
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+HERE = os.path.dirname(os.path.abspath(__file__))
+if HERE not in sys.path:
+    sys.path.insert(0, HERE)
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA GPU (B300, sm_103a)")
+    config.addinivalue_line("markers", "slow: full-size workload (GPU); minutes, not seconds")
+
+
+def pytest_collection_modifyitems(config, items):
+    # the allocation-free entry point's test file sorts last; keep file order otherwise
+    items.sort(key=lambda it: os.path.basename(str(it.fspath)).startswith("test_zz"))
