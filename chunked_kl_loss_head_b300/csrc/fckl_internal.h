@@ -1,0 +1,94 @@
+// fckl_internal.h -- declarations shared by the host API and the kernel files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/fckl.h"
+
+namespace fckl {
+
+constexpr int kTileM = 128;   // rows (tokens) of one logit tile
+constexpr int kTileV = 256;   // vocab columns of one logit tile (forward partial granularity)
+constexpr int kCtrlBytes = 256;
+
+// First bytes of the workspace: status word and scalars shared between kernels.
+struct Ctrl {
+  int32_t status;        // first device-detected fckl_status (0 = none)
+  int32_t pad0;
+  int64_t n_valid;       // N of the last reduction
+  float grad_alpha;      // g / (tau * N) for the backward (0 when N = 0)
+  float pad1;
+  double loss_sum;       // sum of valid loss_t of the last forward
+};
+
+// Records `code` as the workspace status unless one is already recorded.
+__device__ __forceinline__ void set_status(Ctrl* ctrl, int code) {
+  atomicCAS(&ctrl->status, 0, code);
+}
+
+// Per-chunk scratch carved out of the workspace.
+struct ChunkScratch {
+  int32_t* sidx;    // [C, K] teacher ids of each row, ascending (bad ids -> INT32_MAX)
+  float* sp;        // [C, K] teacher p, permuted like sidx
+  float* slogp;     // [C, K] teacher log p, permuted like sidx
+  float* zk;        // [C, K] student logit at sidx (forward)
+  float2* part;     // [C, nvt] per (row, 256-wide vocab tile): (max, sum) in log2 units
+  void* G;          // [C, S] gradient tile stripe (bf16 for bf16 work, f32 for f32 work)
+  float* dHacc;     // [C, d] fp32 dH accumulator (bf16 work only)
+};
+
+// ---- row kernels (fckl_rowops.cu) --------------------------------------------------------
+cudaError_t launch_prep(const int32_t* idx, const float* logits, int64_t rows, int32_t K, int64_t V,
+                        float tau, ChunkScratch s, Ctrl* ctrl, cudaStream_t st);
+cudaError_t launch_combine(const float2* part, int nvt, const float* zk, const float* sp,
+                           const float* slogp, const uint8_t* valid, int64_t rows, int32_t K,
+                           float tau, float* lse, float* row_loss, cudaStream_t st);
+cudaError_t launch_loss_reduce(const float* row_loss, const uint8_t* valid, int64_t T, float* loss,
+                               Ctrl* ctrl, cudaStream_t st);
+cudaError_t launch_grad_scale(const uint8_t* valid, int64_t T, float tau, float grad_loss,
+                              const float* grad_scale, Ctrl* ctrl, cudaStream_t st);
+cudaError_t launch_f32_to_bf16(const float* src, void* dst, int64_t n, cudaStream_t st);
+
+// ---- fp32 CUDA-core path (fckl_simt.cu) --------------------------------------------------
+cudaError_t launch_simt_fwd_tiles(const float* Hc, const float* W, int64_t rows, int64_t d, int64_t V,
+                                  float tau, const int32_t* sidx, int32_t K, float* zk, float2* part,
+                                  int nvt, cudaStream_t st);
+cudaError_t launch_simt_bwd_tiles(const float* Hc, const float* W, int64_t rows, int64_t d, int64_t V,
+                                  int64_t s0, int64_t S, float tau, const int32_t* sidx,
+                                  const float* sp, int32_t K, const float* lse, const uint8_t* valid,
+                                  const Ctrl* ctrl, float* G, cudaStream_t st);
+// C[M, N] = beta * C + sum_k A(m, k) B(k, n), A(m,k) = A[m*sam + k*sak], B(k,n) = B[k*sbk + n*sbn]
+cudaError_t launch_simt_gemm(const float* A, int64_t sam, int64_t sak, const float* B, int64_t sbk,
+                             int64_t sbn, float* C, int64_t ldc, int64_t M, int64_t N, int64_t K,
+                             int beta, cudaStream_t st);
+
+// ---- bf16 tensor-core path (fckl_tc.cu) --------------------------------------------------
+cudaError_t tc_fwd_tiles(const void* Hc, const void* W, int64_t rows, int64_t d, int64_t V,
+                         float tau, const int32_t* sidx, int32_t K, float* zk, float2* part, int nvt,
+                         Ctrl* ctrl, int num_sms, cudaStream_t st);
+cudaError_t tc_bwd_tiles(const void* Hc, const void* W, int64_t rows, int64_t d, int64_t V,
+                         int64_t s0, int64_t S, float tau, const int32_t* sidx, const float* sp,
+                         int32_t K, const float* lse, const uint8_t* valid, Ctrl* ctrl,
+                         void* G, int64_t ldG, int num_sms, cudaStream_t st);
+// dW[s0:s0+S, :] (+)= G^T . Hc    (G is [rows, ldG] bf16, first S columns used)
+cudaError_t tc_dW(const void* G, int64_t ldG, const void* Hc, int64_t rows, int64_t d, int64_t S,
+                  float* dW_stripe, int accumulate, Ctrl* ctrl, int num_sms, cudaStream_t st);
+// dH accumulator: acc[rows, d] (+)= G . W[s0:s0+S, :]; when `out_bf16` is non-null the final
+// sum is written there as bf16 instead of back to acc.
+cudaError_t tc_dH(const void* G, int64_t ldG, const void* W_stripe, int64_t rows, int64_t d,
+                  int64_t S, float* acc, int accumulate, void* out_bf16, Ctrl* ctrl, int num_sms,
+                  cudaStream_t st);
+cudaError_t tc_debug_gemm(const void* A, const void* B, float* D, int64_t M, int64_t N, int64_t K,
+                          int a_mn, int b_mn, int num_sms, cudaStream_t st);
+
+// ---- host helpers (fckl_api.cu) ----------------------------------------------------------
+bool encode_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                         uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer);
+void count_launch(fckl_kernel_class cls);
+void prof_begin(fckl_kernel_class cls, cudaStream_t st);
+void prof_end(fckl_kernel_class cls, cudaStream_t st);
+
+}  // namespace fckl

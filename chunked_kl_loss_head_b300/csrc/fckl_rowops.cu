@@ -1,0 +1,223 @@
+// fckl_rowops.cu -- the per-row steps of the loss: teacher preparation, the per-row
+// combine of vocab-tile partials into lse_t and loss_t, the fixed-order mean over rows,
+// the gradient scale g / (tau N) and the final bf16 cast of dH.
+#include <cuda_bf16.h>
+
+#include <cfloat>
+#include <climits>
+
+#include "fckl_internal.h"
+
+namespace fckl {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr float kLn2 = 0.6931471805599453f;
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  return v;
+}
+
+// Teacher preparation, one warp per row (the teacher's top-K cache, getaibook.com,
+// "Preparing Offline Top-K Logits"): p = softmax(topk_logits / tau) over the K cached
+// ids, log p alongside, and the (id, p, log p) triples sorted by id so the logit-tile
+// epilogues can walk a row's ids in vocabulary order.  Ids outside [0, V) are recorded
+// as FCKL_ERR_BAD_INDEX and replaced by INT32_MAX with p = 0, so no later step can use
+// them as an address or match them to a column.  zk (the student logits at the ids) is
+// cleared for the forward tiles to fill.
+__global__ void prep_kernel(const int32_t* __restrict__ idx, const float* __restrict__ logits,
+                            int64_t rows, int K, int64_t V, float tau, int32_t* __restrict__ sidx,
+                            float* __restrict__ sp, float* __restrict__ slogp, float* __restrict__ zk,
+                            Ctrl* ctrl) {
+  extern __shared__ int32_t sh_ids[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + warp;
+  if (row >= rows) return;
+  int32_t* ids = sh_ids + warp * K;
+  const int32_t* irow = idx + row * K;
+  const float* lrow = logits + row * K;
+
+  float amax = -INFINITY;
+  bool bad = false;
+  for (int k = lane; k < K; k += 32) {
+    int32_t id = irow[k];
+    if (id < 0 || static_cast<int64_t>(id) >= V) {
+      bad = true;
+      id = INT32_MAX;
+    }
+    ids[k] = id;
+    amax = fmaxf(amax, lrow[k] / tau);
+  }
+  if (__any_sync(kFull, bad) && lane == 0) set_status(ctrl, FCKL_ERR_BAD_INDEX);
+  amax = warp_max(amax);
+  float sum = 0.f;
+  for (int k = lane; k < K; k += 32) sum += expf(lrow[k] / tau - amax);
+  sum = warp_sum(sum);
+  const float lse_a = amax + logf(sum);
+  __syncwarp();
+
+  for (int k = lane; k < K; k += 32) {
+    const int32_t id = ids[k];
+    int rank = 0;
+    for (int j = 0; j < K; ++j) {
+      const int32_t o = ids[j];
+      rank += (o < id) | ((o == id) & (j < k));
+    }
+    const float lp = lrow[k] / tau - lse_a;
+    const int64_t o = row * K + rank;
+    sidx[o] = id;
+    slogp[o] = lp;
+    sp[o] = (id == INT32_MAX) ? 0.f : expf(lp);
+    zk[o] = 0.f;
+  }
+}
+
+// One warp per row: merge the (max, sum) partials of every 256-wide vocab tile into the
+// row's logsumexp, then loss_t = sum_k p_k (log p_k - s_k + lse_t) with s_k = z_k / tau.
+// Partials are in base-2 units (u = z * log2(e) / tau).
+__global__ void combine_kernel(const float2* __restrict__ part, int nvt, const float* __restrict__ zk,
+                               const float* __restrict__ sp, const float* __restrict__ slogp,
+                               const uint8_t* __restrict__ valid, int64_t rows, int K, float tau,
+                               float* __restrict__ lse, float* __restrict__ row_loss) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + warp;
+  if (row >= rows) return;
+  const float2* pr = part + row * nvt;
+  float m = -INFINITY;
+  for (int j = lane; j < nvt; j += 32) m = fmaxf(m, pr[j].x);
+  m = warp_max(m);
+  float s = 0.f;
+  for (int j = lane; j < nvt; j += 32) {
+    const float2 q = pr[j];
+    s += q.y * exp2f(q.x - m);
+  }
+  s = warp_sum(s);
+  const float l = (m + log2f(s)) * kLn2;
+  float acc = 0.f;
+  const bool ok = valid[row] != 0;
+  if (ok) {
+    const int64_t b = row * K;
+    for (int k = lane; k < K; k += 32) acc += sp[b + k] * (slogp[b + k] - zk[b + k] / tau + l);
+  }
+  acc = warp_sum(acc);
+  if (lane == 0) {
+    lse[row] = l;
+    row_loss[row] = ok ? acc : 0.f;
+  }
+}
+
+constexpr int kReduceThreads = 1024;
+
+// Block-wide fixed-order sums (one block): each thread adds a strided slice in fp64, then a
+// fixed binary tree.  The result depends only on T, never on the chunk size.
+__device__ void block_sum2(double& s, long long& n) {
+  __shared__ double sh_s[kReduceThreads];
+  __shared__ long long sh_n[kReduceThreads];
+  sh_s[threadIdx.x] = s;
+  sh_n[threadIdx.x] = n;
+  __syncthreads();
+  for (int w = kReduceThreads / 2; w > 0; w >>= 1) {
+    if (threadIdx.x < w) {
+      sh_s[threadIdx.x] += sh_s[threadIdx.x + w];
+      sh_n[threadIdx.x] += sh_n[threadIdx.x + w];
+    }
+    __syncthreads();
+  }
+  s = sh_s[0];
+  n = sh_n[0];
+}
+
+__global__ void __launch_bounds__(kReduceThreads) loss_reduce_kernel(const float* __restrict__ row_loss,
+                                                                    const uint8_t* __restrict__ valid,
+                                                                    int64_t T, float* loss, Ctrl* ctrl) {
+  double s = 0.0;
+  long long n = 0;
+  for (int64_t i = threadIdx.x; i < T; i += kReduceThreads) {
+    const bool ok = valid[i] != 0;
+    s += ok ? static_cast<double>(row_loss[i]) : 0.0;
+    n += ok;
+  }
+  block_sum2(s, n);
+  if (threadIdx.x == 0) {
+    ctrl->n_valid = n;
+    ctrl->loss_sum = s;
+    *loss = n > 0 ? static_cast<float>(s / static_cast<double>(n)) : 0.f;
+  }
+}
+
+__global__ void __launch_bounds__(kReduceThreads) grad_scale_kernel(const uint8_t* __restrict__ valid, int64_t T,
+                                                                   float tau, float grad_loss,
+                                                                   const float* grad_scale, Ctrl* ctrl) {
+  double s = 0.0;
+  long long n = 0;
+  for (int64_t i = threadIdx.x; i < T; i += kReduceThreads) n += valid[i] != 0;
+  block_sum2(s, n);
+  if (threadIdx.x == 0) {
+    double g = grad_loss;
+    if (grad_scale) g *= static_cast<double>(*grad_scale);
+    ctrl->n_valid = n;
+    ctrl->grad_alpha = n > 0 ? static_cast<float>(g / (static_cast<double>(tau) * static_cast<double>(n))) : 0.f;
+  }
+}
+
+__global__ void f32_to_bf16_kernel(const float4* __restrict__ src, __nv_bfloat162* __restrict__ dst, int64_t n4) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n4;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float4 v = src[i];
+    dst[2 * i] = __floats2bfloat162_rn(v.x, v.y);
+    dst[2 * i + 1] = __floats2bfloat162_rn(v.z, v.w);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_prep(const int32_t* idx, const float* logits, int64_t rows, int32_t K, int64_t V,
+                        float tau, ChunkScratch s, Ctrl* ctrl, cudaStream_t st) {
+  constexpr int warps = 4;
+  const unsigned grid = static_cast<unsigned>((rows + warps - 1) / warps);
+  prep_kernel<<<grid, warps * 32, warps * K * sizeof(int32_t), st>>>(idx, logits, rows, K, V, tau, s.sidx, s.sp,
+                                                                     s.slogp, s.zk, ctrl);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const float2* part, int nvt, const float* zk, const float* sp, const float* slogp,
+                           const uint8_t* valid, int64_t rows, int32_t K, float tau, float* lse,
+                           float* row_loss, cudaStream_t st) {
+  constexpr int warps = 8;
+  const unsigned grid = static_cast<unsigned>((rows + warps - 1) / warps);
+  combine_kernel<<<grid, warps * 32, 0, st>>>(part, nvt, zk, sp, slogp, valid, rows, K, tau, lse, row_loss);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_loss_reduce(const float* row_loss, const uint8_t* valid, int64_t T, float* loss, Ctrl* ctrl,
+                               cudaStream_t st) {
+  loss_reduce_kernel<<<1, kReduceThreads, 0, st>>>(row_loss, valid, T, loss, ctrl);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_grad_scale(const uint8_t* valid, int64_t T, float tau, float grad_loss, const float* grad_scale,
+                              Ctrl* ctrl, cudaStream_t st) {
+  grad_scale_kernel<<<1, kReduceThreads, 0, st>>>(valid, T, tau, grad_loss, grad_scale, ctrl);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_f32_to_bf16(const float* src, void* dst, int64_t n, cudaStream_t st) {
+  const int64_t n4 = n / 4;  // n is a multiple of 8 (d % 8 == 0)
+  const int threads = 256;
+  int64_t blocks = (n4 + threads - 1) / threads;
+  if (blocks > 148 * 16) blocks = 148 * 16;
+  if (blocks < 1) blocks = 1;
+  f32_to_bf16_kernel<<<static_cast<unsigned>(blocks), threads, 0, st>>>(
+      reinterpret_cast<const float4*>(src), reinterpret_cast<__nv_bfloat162*>(dst), n4);
+  return cudaGetLastError();
+}
+
+}  // namespace fckl

@@ -1,0 +1,161 @@
+/*
+ * fckl.h -- C-ABI of the fused chunked KL distillation loss for NVIDIA B300 (sm_103a).
+ *
+ * The operation.  A student is distilled from a teacher whose output was cached
+ * offline as its top-K (id, logit) pairs per token position (axbrief.com,
+ * "Breaking the Bottleneck with Offline Caching and Chunked Loss";
+ * getaibook.com, "Preparing Offline Top-K Logits").  The loss is the KL
+ * divergence between teacher and student (getaibook.com, "Configuring Fused
+ * Chunked KL Loss"), with the student's output projection (lm_head) folded
+ * into it, so the [tokens x vocab] logit grid is never built, and the
+ * sequence is processed one chunk at a time (calcaas.com, "What actually
+ * changed?").  The pages print no formula; this library computes, for every
+ * row t with the tempered student logits s_t = (H_t . W^T) / tau:
+ *
+ *   log p_tk = a_tk - logsumexp_k(a_t),   a_tk = topk_logits_tk / tau
+ *   lse_t    = logsumexp_v(s_tv)
+ *   loss_t   = sum_k p_tk (log p_tk - s_t,idx_tk + lse_t)       (forward KL)
+ *   loss     = sum_{valid t} loss_t / N,     N = number of valid rows
+ *   dz_tv    = g (exp(s_tv - lse_t) - sum_k p_tk [idx_tk = v]) / (tau N)
+ *   dH = dz . W,   dW = dz^T . H
+ *
+ * with g = grad_loss (times *grad_scale when given); N = 0 gives loss 0 and
+ * zero gradients.  Duplicate ids in a row add up termwise.
+ *
+ * Conventions shared by every call:
+ *  - All tensors are row-major and contiguous, on the current CUDA device.
+ *    H[T, d] and W[V, d] hold `dtype` elements; dH[T, d] is written in the
+ *    same dtype; dW[V, d] is float32.  topk_idx[T, K] is int32 in [0, V);
+ *    topk_logits[T, K] float32; valid[T] uint8 (nonzero = the row counts);
+ *    lse[T] and row_loss[T] float32.
+ *  - The caller owns every buffer.  The library never allocates device
+ *    memory: scratch space is the caller's workspace `ws` of at least
+ *    fckl_workspace_size(...) bytes, 256-byte aligned.  No state is kept
+ *    between calls except the optional launch counters and profiling events
+ *    of the instrumentation calls at the end of this header.
+ *  - Every compute call is asynchronous and stream-ordered on `stream` (a
+ *    cudaStream_t; NULL = the legacy default stream).  Calls that share a
+ *    workspace must be ordered on the GPU.
+ *  - Argument errors are returned before anything is launched.  Errors the
+ *    GPU detects (an id outside [0, V), a wait that timed out) are recorded in
+ *    a status word inside the workspace; read them with fckl_get_error after
+ *    the work, no kernel ever traps.  fckl_forward clears that word first.
+ *  - bf16 work runs on tcgen05 tensor cores (bf16 inputs, fp32 accumulation)
+ *    and needs d % 8 == 0 and 16-byte aligned H, W, dH; float32 work runs on
+ *    fp32 CUDA cores.
+ */
+#ifndef FCKL_H_
+#define FCKL_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FCKL_API __attribute__((visibility("default")))
+#else
+#define FCKL_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FCKL_OK = 0,
+  FCKL_ERR_INVALID_ARG = 1, /* a null pointer, a size or tau out of range */
+  FCKL_ERR_UNSUPPORTED = 2, /* valid arguments this build cannot run (alignment, K limit, device) */
+  FCKL_ERR_WORKSPACE = 3,   /* ws is null, too small or not 256-byte aligned */
+  FCKL_ERR_CUDA = 4,        /* a CUDA runtime call failed (launch, attribute, memset) */
+  FCKL_ERR_BAD_INDEX = 5,   /* a teacher id outside [0, V) (reported by fckl_get_error) */
+  FCKL_ERR_TIMEOUT = 6      /* a bounded on-device wait gave up (reported by fckl_get_error) */
+} fckl_status;
+
+typedef enum { FCKL_F32 = 0, FCKL_BF16 = 1 } fckl_dtype;
+
+/* Largest K (teacher ids per row) the kernels accept. */
+#define FCKL_MAX_K 1024
+
+/* Bytes of workspace fckl_forward and fckl_backward need for these sizes (the
+ * same for both).  It grows with the chunk (per-chunk scratch of
+ * O(chunk * vocab tile)), never with T * V; 0 for invalid sizes. */
+FCKL_API size_t fckl_workspace_size(int64_t T, int64_t d, int64_t V, int32_t K, int64_t chunk,
+                           fckl_dtype dtype);
+
+/* Forward: the mean loss and the per-row student logsumexp.
+ * Processes the T rows `chunk` rows at a time; for each chunk the logit tiles
+ * H_chunk . W^T are formed tile by tile and reduced on chip to a running
+ * max / sum per row and to the student logits at the teacher's ids, so the
+ * result does not depend on `chunk`.
+ *   loss     device float32 scalar, written (0 when no row is valid)
+ *   lse      device float32 [T], written for every row, ignored rows included
+ *            (logsumexp of s_t = H_t . W^T / tau; fckl_backward takes it back)
+ *   row_loss device float32 [T] or NULL: loss_t for valid rows, 0 for ignored
+ * Returns FCKL_OK once the work is queued on `stream`. */
+FCKL_API fckl_status fckl_forward(const void* H, const void* W, const int32_t* topk_idx,
+                         const float* topk_logits, const uint8_t* valid, int64_t T, int64_t d,
+                         int64_t V, int32_t K, float tau, int64_t chunk, fckl_dtype dtype,
+                         float* loss, float* lse, float* row_loss, void* ws, size_t ws_bytes,
+                         void* stream);
+
+/* Backward: dH and dW of g * loss, recomputing the logit tiles chunk by chunk
+ * (the extra projection work in the backward pass that chunking costs,
+ * axbrief.com, "Breaking the Bottleneck with Offline Caching and Chunked Loss").
+ *   lse        device float32 [T] from fckl_forward with the same inputs
+ *   grad_loss  host scalar g (dL/dloss)
+ *   grad_scale device float32 scalar or NULL; when given, g is multiplied by it
+ *   dH         device [T, d] in `dtype`, overwritten; rows of ignored tokens are 0
+ *   dW         device float32 [V, d], overwritten
+ * Returns FCKL_OK once the work is queued on `stream`. */
+FCKL_API fckl_status fckl_backward(const void* H, const void* W, const int32_t* topk_idx,
+                          const float* topk_logits, const uint8_t* valid, int64_t T, int64_t d,
+                          int64_t V, int32_t K, float tau, int64_t chunk, fckl_dtype dtype,
+                          const float* lse, float grad_loss, const float* grad_scale, void* dH,
+                          float* dW, void* ws, size_t ws_bytes, void* stream);
+
+/* Waits for `stream`, then returns and clears the status word the GPU wrote in
+ * the workspace (FCKL_OK, FCKL_ERR_BAD_INDEX or FCKL_ERR_TIMEOUT), or
+ * FCKL_ERR_CUDA when the wait or the copy itself failed. */
+FCKL_API fckl_status fckl_get_error(void* ws, void* stream);
+
+/* A static description of a status code. */
+FCKL_API const char* fckl_status_string(fckl_status status);
+
+/* ---- instrumentation (host-side counters; off unless enabled) ---------------------------
+ * Kernel classes, in the order the path runs them. */
+typedef enum {
+  FCKL_K_PREP = 0,     /* teacher softmax + id sort, per chunk */
+  FCKL_K_FWD_TILES,    /* logit tiles + online max/sum + gather (forward) */
+  FCKL_K_COMBINE,      /* per-row lse and loss_t from the tile partials */
+  FCKL_K_REDUCE,       /* fixed-order mean over rows; N and the gradient scale */
+  FCKL_K_BWD_TILES,    /* recomputed logit tiles -> gradient tile G (backward) */
+  FCKL_K_DW,           /* dW[stripe] (+)= G^T . H_chunk */
+  FCKL_K_DH,           /* dH_chunk (+)= G . W[stripe] */
+  FCKL_K_OTHER,        /* memsets and casts */
+  FCKL_K_NUM_CLASSES
+} fckl_kernel_class;
+
+/* Number of kernels this library has launched since load (all classes). */
+FCKL_API int64_t fckl_launch_count(void);
+
+/* When on, every launch is bracketed by CUDA events on its stream so that
+ * fckl_profile_read can report per-class device time.  Off by default. */
+FCKL_API void fckl_profile_enable(int on);
+
+/* Synchronizes the recorded events and returns, for one class, the number of
+ * launches and their summed device time (ms) since the last reset; resets
+ * when `reset` is nonzero.  Returns FCKL_ERR_INVALID_ARG for a bad class. */
+FCKL_API fckl_status fckl_profile_read(int32_t kernel_class, int64_t* launches, double* total_ms, int reset);
+
+/* Test hook for the tcgen05 GEMM engine: D[M, N] (float32, row-major, ldd = N)
+ * = A . B with bf16 operands on the same tensor-core path the loss uses.
+ * a_mn == 0: A is [M, K] (K contiguous); a_mn == 1: A is stored [K, M].
+ * b_mn == 0: B is stored [N, K] (so D = A . B^T); b_mn == 1: B is stored [K, N].
+ * M, N, K >= 1; M or N contiguous extents need multiples of 8 elements. */
+FCKL_API fckl_status fckl_debug_gemm_bf16(const void* A, const void* B, float* D, int64_t M, int64_t N,
+                                 int64_t K, int32_t a_mn, int32_t b_mn, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FCKL_H_ */

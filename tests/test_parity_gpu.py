@@ -1,0 +1,191 @@
+"""CUDA path vs the fp64 oracle, element by element, on seeded inputs that span
+several tiles, several chunks and vocab stripes, and ragged tails, plus the
+degenerate cases of the loss.  Everything goes through the C-ABI."""
+
+import numpy as np
+import pytest
+import torch
+
+from chunked_kl_loss_head_b300 import api
+from gen import CONFIGS, make_inputs, make_small
+from helpers import TOL, oracle_of, rel, rel_max, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+def run_gpu(x, chunk, grad_loss=1.0):
+    cfg = x["cfg"]
+    d = to_device(x)
+    T, dd = d["H"].shape
+    V, K = d["W"].shape[0], d["topk_idx"].shape[1]
+    ws = api.workspace(T, dd, V, K, chunk, d["H"].dtype)
+    loss, lse, rl = api.forward(d["H"], d["W"], d["topk_idx"], d["topk_logits"], d["valid"], cfg.tau, chunk, ws=ws,
+                                want_row_loss=True)
+    dH, dW = api.backward(d["H"], d["W"], d["topk_idx"], d["topk_logits"], d["valid"], lse, cfg.tau, chunk,
+                          grad_loss=grad_loss, ws=ws)
+    status = api.fckl_get_error(ws)
+    torch.cuda.synchronize()
+    return dict(loss=loss.item(), lse=lse.cpu().numpy(), row_loss=rl.cpu().numpy(),
+                dH=dH.float().cpu().numpy(), dW=dW.cpu().numpy(), status=status)
+
+
+def check(x, got, grad_loss=1.0, label=""):
+    tol = TOL[x["cfg"].dtype]
+    ref = oracle_of(x, grad=grad_loss)
+    assert got["status"] == 0, api.fckl_status_string(got["status"])
+    errs = dict(loss=rel(got["loss"], ref["loss"]), lse=rel_max(got["lse"], ref["lse"]),
+                row_loss=rel_max(got["row_loss"], ref["row_loss"]), dH=rel_max(got["dH"], ref["dH"]),
+                dW=rel_max(got["dW"], ref["dW"]))
+    print(label, {k: f"{v:.2e}" for k, v in errs.items()})
+    assert errs["loss"] <= tol["loss"], errs
+    assert errs["lse"] <= tol["loss"], errs
+    assert errs["row_loss"] <= tol["loss"], errs
+    assert errs["dH"] <= tol["grad"], errs
+    assert errs["dW"] <= tol["grad"], errs
+    valid = np.asarray(x["valid"]).astype(bool)
+    assert np.all(got["dH"][~valid] == 0.0), "ignored rows must have dH exactly 0"
+    assert np.all(got["row_loss"][~valid] == 0.0)
+    return errs
+
+
+# ------------------------------------------------------------------------------ GEMM engine
+
+
+@pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 0), (1, 1)])
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (304, 520, 200), (1000, 2880, 136), (8, 8, 8)])
+def test_engine_gemm_layouts(a_mn, b_mn, M, N, K):
+    g = torch.Generator().manual_seed(M * 7 + N + K)
+    A = torch.randn((K, M) if a_mn else (M, K), generator=g).to(torch.bfloat16)
+    B = torch.randn((K, N) if b_mn else (N, K), generator=g).to(torch.bfloat16)
+    A64 = A.double().T if a_mn else A.double()
+    B64 = B.double() if b_mn else B.double().T
+    ref = (A64 @ B64).numpy()
+    D = torch.full((M, N), float("nan"), device="cuda")
+    api.fckl_debug_gemm_bf16(A.cuda(), B.cuda(), D, M, N, K, a_mn, b_mn)
+    torch.cuda.synchronize()
+    err = rel_max(D.cpu().numpy(), ref)
+    assert err <= 1e-5, err
+
+
+# ------------------------------------------------------------------------------ loss parity
+
+
+@pytest.mark.parametrize("chunk", [64, 16, 7])
+def test_tiny_fp32_config(chunk):
+    x = make_inputs(CONFIGS["tiny_fp32"])
+    check(x, run_gpu(x, chunk), label=f"tiny_fp32 chunk={chunk}")
+
+
+def test_fp32_several_chunks_and_stripes():
+    x = make_small(T=4200, d=40, V=10000, K=5, tau=1.3, dtype="f32", seed=3, mask="random", mask_frac=0.1)
+    check(x, run_gpu(x, 4096), label="f32 multi-chunk/stripe")
+
+
+def test_bf16_several_chunks_and_stripes():
+    # chunk 4096 -> stripes of 8192 vocab columns: 3 stripes, the last ragged (3616 columns)
+    x = make_small(T=5000, d=64, V=20000, K=13, tau=1.5, dtype="bf16", seed=1, mask="random", mask_frac=0.1)
+    check(x, run_gpu(x, 4096), label="bf16 multi-chunk/stripe")
+
+
+@pytest.mark.parametrize("chunk", [128, 100, 1000])
+def test_bf16_ragged_tiles(chunk):
+    x = make_small(T=300, d=200, V=1000, K=7, tau=0.8, dtype="bf16", seed=2, mask="random", mask_frac=0.2)
+    check(x, run_gpu(x, chunk), label=f"bf16 ragged chunk={chunk}")
+
+
+def test_bf16_uniform_ids_onehot_teacher():
+    x = make_small(T=700, d=128, V=3000, K=10, tau=1.0, dtype="bf16", seed=4, ids="uniform", onehot_frac=0.1,
+                   logit_offset=10.0)
+    check(x, run_gpu(x, 512), label="bf16 uniform ids / one-hot")
+
+
+def test_bf16_chunk_invariance_of_loss():
+    x = make_small(T=5000, d=64, V=20000, K=13, tau=1.5, dtype="bf16", seed=1, mask="random", mask_frac=0.1)
+    runs = [run_gpu(x, c) for c in (4096, 1000, 5000, 333)]
+    for r in runs[1:]:
+        assert r["loss"] == runs[0]["loss"], "loss depends on the chunk size"
+        np.testing.assert_array_equal(r["lse"], runs[0]["lse"])
+        np.testing.assert_array_equal(r["row_loss"], runs[0]["row_loss"])
+        assert rel_max(r["dW"], runs[0]["dW"]) <= 1e-3
+        assert rel_max(r["dH"], runs[0]["dH"]) <= 1e-2
+
+
+# ------------------------------------------------------------------------------ edge cases
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_no_valid_rows(dtype):
+    x = make_small(T=200, d=64, V=600, K=4, tau=1.0, dtype=dtype, seed=6)
+    x["valid"] = np.zeros(200, np.uint8)
+    got = run_gpu(x, 128)
+    assert got["status"] == 0
+    assert got["loss"] == 0.0
+    assert not got["dH"].any() and not got["dW"].any()
+    ref = oracle_of(x, want_grads=False)
+    assert rel_max(got["lse"], ref["lse"]) <= TOL[dtype]["loss"]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("T", [1, 5, 129])
+def test_short_inputs(dtype, T):
+    x = make_small(T=T, d=32, V=300, K=3, tau=2.0, dtype=dtype, seed=7 + T)
+    check(x, run_gpu(x, 64), label=f"{dtype} T={T}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_k_equals_one_and_v(dtype):
+    x = make_small(T=50, d=16, V=64, K=1, tau=1.0, dtype=dtype, seed=8)
+    check(x, run_gpu(x, 32), label=f"{dtype} K=1")
+    x = make_small(T=50, d=16, V=64, K=64, tau=1.7, dtype=dtype, seed=9, ids="uniform")
+    check(x, run_gpu(x, 32), label=f"{dtype} K=V")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_duplicate_ids_add_up(dtype):
+    x = make_small(T=40, d=24, V=500, K=6, tau=1.0, dtype=dtype, seed=10)
+    x["topk_idx"][:, 1] = x["topk_idx"][:, 0]
+    x["topk_idx"][3, :] = 7
+    check(x, run_gpu(x, 16), label=f"{dtype} duplicate ids")
+
+
+def test_grad_scale_and_grad_loss():
+    x = make_small(T=256, d=64, V=800, K=5, tau=1.0, dtype="bf16", seed=11, mask="random", mask_frac=0.1)
+    a = run_gpu(x, 128, grad_loss=2.5)
+    check(x, a, grad_loss=2.5, label="grad_loss=2.5")
+    d = to_device(x)
+    ws = api.workspace(256, 64, 800, 5, 128, torch.bfloat16)
+    loss, lse = api.forward(d["H"], d["W"], d["topk_idx"], d["topk_logits"], d["valid"], 1.0, 128, ws=ws)
+    gs = torch.tensor(2.5, device="cuda")
+    dH, dW = api.backward(d["H"], d["W"], d["topk_idx"], d["topk_logits"], d["valid"], lse, 1.0, 128, 1.0, ws=ws,
+                          grad_scale=gs)
+    np.testing.assert_array_equal(dW.cpu().numpy(), a["dW"])
+    np.testing.assert_array_equal(dH.float().cpu().numpy(), a["dH"])
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_bad_index_reports_status(dtype):
+    x = make_small(T=100, d=32, V=400, K=4, tau=1.0, dtype=dtype, seed=12)
+    x["topk_idx"][5, 2] = 400
+    x["topk_idx"][9, 0] = -3
+    got = run_gpu(x, 64)
+    assert got["status"] == 5
+    assert np.isfinite(got["lse"]).all()
+    # the status word is cleared by the read
+    d = to_device(x)
+    ws = api.workspace(100, 32, 400, 4, 64, d["H"].dtype)
+    assert api.fckl_get_error(ws) == 0
+
+
+def test_autograd_module_matches_abi():
+    from chunked_kl_loss_head_b300 import FusedChunkedKLLoss
+
+    x = make_small(T=300, d=64, V=900, K=6, tau=1.5, dtype="f32", seed=13, mask="random", mask_frac=0.1)
+    d = to_device(x)
+    H = d["H"].clone().requires_grad_(True)
+    W = d["W"].clone().requires_grad_(True)
+    loss = FusedChunkedKLLoss(tau=1.5, chunk=128)(H, W, d["topk_idx"], d["topk_logits"], d["valid"])
+    (3.0 * loss).backward()
+    ref = oracle_of(x, grad=3.0)
+    assert rel(loss.item(), ref["loss"]) <= 1e-5
+    assert rel_max(H.grad.cpu().numpy(), ref["dH"]) <= 1e-4
+    assert rel_max(W.grad.cpu().numpy(), ref["dW"]) <= 1e-4
