@@ -1,0 +1,364 @@
+"""Benchmark of the fused chunked KL loss (forward + backward) on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config gptoss_bf16] [--chunk 4096]
+    python bench.py --impl reference ...      # the fp64 oracle on the host cores
+
+One step = fckl_forward + fckl_backward over one batch of the workload (all
+T tokens): loss, per-row logsumexp, dH and dW.  Inputs are synthetic (seeded
+generators, shapes of the pages' workloads) and larger than the 126 MB L2.
+Prints one JSON line (rank 0).  Under torchrun each rank runs its own batch
+(weak scaling, no collective on the data path); the time is the max over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "top-K KL fwd+bwd tokens/s; % of BF16 tensor peak; peak device GiB"
+DEFAULT_CONFIG = "gptoss_bf16"
+FALLBACK_PEAKS = dict(hbm_gbs=6400.0, bf16_tflops=1800.0, bf16_tflops_sustained=1400.0, source="fallback")
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        d["source"] = "measured"
+        return d
+    return dict(FALLBACK_PEAKS)
+
+
+def algorithmic_flops(T, d, V, n_valid):
+    """Forward logits for every row (2dV); backward recompute + dH + dW for valid rows (6dV)."""
+    return 8.0 * d * V * n_valid + 2.0 * d * V * (T - n_valid)
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")), ws
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.f = None
+
+    def __enter__(self):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self.f.flush()
+
+    def summary(self):
+        rows = []
+        try:
+            for line in open(self.f.name):
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        finally:
+            os.unlink(self.f.name)
+        if not rows:
+            return dict(sm_mhz=None, sm_max_mhz=None, reasons=["unsampled"])
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        pw = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        load = [s for s in sm if s > 0.5 * (max(mx) if mx else 1)] or sm
+        return dict(sm_mhz=float(np.median(load)) if load else None, sm_max_mhz=max(mx) if mx else None,
+                    power_w_max=max(pw) if pw else None, samples=len(rows), reasons=reasons)
+
+
+def cpu_oracle_rate(cfg, W_bits, rows, reps=1):
+    """Oracle fwd+bwd (fp64, full-vocab logit rows, analytic dH / dW) on `rows` rows of
+    the workload; returns (tokens/s, seconds)."""
+    from gen import bf16_bits_to_f32, make_rows, valid_mask
+    from oracle import fwd_bwd
+
+    x = make_rows(cfg, np.arange(rows))
+    H = bf16_bits_to_f32(x["H"]).astype(np.float64) if x["H"].dtype == np.uint16 else x["H"].astype(np.float64)
+    W = bf16_bits_to_f32(W_bits) if W_bits.dtype == np.uint16 else W_bits
+    n_all = int(np.asarray(valid_mask(cfg)).sum())
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        fwd_bwd(H, W, x["topk_idx"], x["topk_logits"], x["valid"], cfg.tau, N=n_all)
+    dt = time.perf_counter() - t0
+    return rows * reps / dt, dt
+
+
+def run_reference(args, cfg):
+    """The oracle as the reference arm: each step is a bounded row sample of the workload."""
+    rank, _, world = dist_env()
+    if world > 1 and rank != 0:
+        return
+    from gen import make_W
+
+    W_bits = make_W(cfg)
+    rows = args.ref_rows
+    cores = len(os.sched_getaffinity(0))
+    for _ in range(args.warmup):
+        cpu_oracle_rate(cfg, W_bits, rows)
+    t = 0.0
+    for _ in range(args.steps):
+        t += cpu_oracle_rate(cfg, W_bits, rows)[1]
+    rate = rows * args.steps / t
+    sample = f"oracle fwd+bwd on rows 0..{rows - 1} of {cfg.name} per step (fp64 numpy/BLAS)"
+    line = dict(impl="reference", metric=METRIC, value=rate, unit="tokens/s", n_gpus=args.gpus, steps=args.steps,
+                warmup=args.warmup, ms_per_step=1e3 * t / args.steps, higher_is_better=True, scaling="weak",
+                vs_baseline=None, dtype="f64", data="synthetic",
+                config=dict(workload=cfg.name, T=cfg.T, d=cfg.d, V=cfg.V, K=cfg.K, tau=cfg.tau),
+                cpu_baseline=dict(value=rate, unit="tokens/s", cores=cores, kind="oracle", sample=sample),
+                e2e=dict(value=rate, unit="tokens/s", h2d_bytes_per_step=0, d2h_bytes_per_step=0))
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="fckl", choices=["fckl", "reference"])
+    ap.add_argument("--config", default=DEFAULT_CONFIG)
+    ap.add_argument("--chunk", type=int, default=0, help="chunk size (default: the workload's first)")
+    ap.add_argument("--cpu-rows", type=int, default=256, help="rows of the oracle CPU-baseline sample")
+    ap.add_argument("--ref-rows", type=int, default=128, help="rows per reference-arm step")
+    ap.add_argument("--shape", default="", help="override T,d,V,K of the workload (e.g. a small ncu case)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+
+    from gen import CONFIGS
+
+    cfg = CONFIGS[args.config]
+    if args.shape:
+        T_, d_, V_, K_ = (int(v) for v in args.shape.split(","))
+        cfg = cfg.with_(name=f"{cfg.name}[T={T_},d={d_},V={V_},K={K_}]", T=T_, d=d_, V=V_, K=K_,
+                        seq_len=min(cfg.seq_len or T_, T_))
+    if args.impl == "reference":
+        run_reference(args, cfg)
+        return
+    if args.warmup < 3:
+        args.warmup = 3  # timing rule: at least three warm-up steps
+
+    import torch
+
+    from chunked_kl_loss_head_b300 import api
+    from gen import make_inputs
+
+    rank, local_rank, world = dist_env()
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    dev = torch.device("cuda", local_rank)
+    chunk = args.chunk or cfg.chunks[0]
+    peaks = load_peaks()
+
+    # ---- inputs (one independent batch per rank), resident in HBM
+    x = make_inputs(cfg.with_(seed=cfg.seed + rank))
+    n_valid = int(x["valid"].sum())
+    T, d, V, K = cfg.T, cfg.d, cfg.V, cfg.K
+    tdt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
+
+    def host(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+        return torch.from_numpy(np.ascontiguousarray(a))
+
+    h = dict(H=host(x["H"]), W=host(x["W"]), topk_idx=host(x["topk_idx"]), topk_logits=host(x["topk_logits"]),
+             valid=host(x["valid"]))
+    del x
+    torch.cuda.reset_peak_memory_stats(dev)
+    free0, _ = torch.cuda.mem_get_info(dev)
+    g = {k: v.to(dev) for k, v in h.items()}
+    ws = api.workspace(T, d, V, K, chunk, tdt, dev)
+    loss = torch.empty((), dtype=torch.float32, device=dev)
+    lse = torch.empty(T, dtype=torch.float32, device=dev)
+    dH = torch.empty((T, d), dtype=tdt, device=dev)
+    dW = torch.empty((V, d), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(src):
+        api.fckl_forward(src["H"], src["W"], src["topk_idx"], src["topk_logits"], src["valid"], cfg.tau, chunk,
+                         loss, lse, None, ws, stream)
+        api.fckl_backward(src["H"], src["W"], src["topk_idx"], src["topk_logits"], src["valid"], cfg.tau, chunk,
+                          lse, 1.0, dH, dW, ws, None, stream)
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        step(g)
+    status = api.fckl_get_error(ws)
+    if status != 0:
+        raise SystemExit(f"device status after warm-up: {api.fckl_status_string(status)}")
+
+    # ---- timed region: K steps, device-resident inputs, per-class kernel events
+    for c in api.KERNEL_CLASSES:
+        api.fckl_profile_read(c, reset=True)
+    api.fckl_profile_enable(True)
+    launches0 = api.fckl_launch_count()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    smi_id = vis.split(",")[local_rank] if vis else str(local_rank)
+    with ClockSampler(smi_id) as clk:
+        barrier()
+        e0.record(stream)
+        for _ in range(args.steps):
+            step(g)
+        e1.record(stream)
+        barrier()
+    api.fckl_profile_enable(False)
+    launches = api.fckl_launch_count() - launches0
+    ms = e0.elapsed_time(e1)
+    per_class = {c: api.fckl_profile_read(c) for c in api.KERNEL_CLASSES}
+    status = api.fckl_get_error(ws)
+    if status != 0:
+        raise SystemExit(f"device status after the timed region: {api.fckl_status_string(status)}")
+    t_max = ms
+    if dist is not None:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_max = float(tt.item())
+    peak_alloc = torch.cuda.max_memory_allocated(dev)
+    free1, _ = torch.cuda.mem_get_info(dev)
+    loss_val = float(loss.item())
+
+    sec_per_step = t_max / 1e3 / args.steps
+    tokens_per_s = world * T / sec_per_step
+    flops = algorithmic_flops(T, d, V, n_valid)
+    tflops = flops / sec_per_step / 1e12
+
+    # ---- roofline of the dominant kernel class (device time from its own events)
+    def class_flops(c):
+        if c == "fwd_tiles":
+            return 2.0 * d * V * T * args.steps
+        if c in ("bwd_tiles", "dW", "dH"):
+            return 2.0 * d * V * n_valid * args.steps
+        return 0.0
+
+    tc_classes = [c for c in ("fwd_tiles", "bwd_tiles", "dW", "dH") if per_class[c][0] > 0]
+    total_ms = sum(v[1] for v in per_class.values())
+    dom = max(tc_classes, key=lambda c: per_class[c][1])
+    dom_launches, dom_ms = per_class[dom]
+    achieved = class_flops(dom) / (dom_ms / 1e3) / 1e12
+    peak_sust = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    peak_burst = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        try:
+            tj = json.load(open(tpath)).get(cfg.name, {}).get(dom)
+            if tj and tj.get("src_sha") == _kernel_src_sha():
+                traffic = tj["bytes_per_launch"]
+        except (ValueError, KeyError):
+            traffic = None
+    roofline = dict(bound="tensor", kernel=dom, achieved=achieved, peak=peak_sust, unit="TFLOP/s",
+                    frac=achieved / peak_sust, traffic=traffic,
+                    peak_note=f"sustained bf16 ({peaks['source']}): kernel timed inside a long step",
+                    launches=dom_launches, avg_launch_ms=dom_ms / max(1, dom_launches),
+                    share_of_device_time=dom_ms / total_ms if total_ms else None,
+                    classes={c: dict(launches=v[0], ms=v[1]) for c, v in per_class.items()})
+
+    # ---- end to end through the public API with host buffers (pinned), loss read back
+    e2e = None
+    if not args.no_e2e:
+        pinned = {k: v.pin_memory() for k, v in h.items()}
+        dst = {k: torch.empty_like(v, device=dev) for k, v in h.items()}
+        h2d = sum(v.numel() * v.element_size() for v in pinned.values())
+        loss_host = torch.empty((), dtype=torch.float32).pin_memory()
+        n_e2e = max(1, min(args.steps, 5))
+        barrier()
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            for k in dst:
+                dst[k].copy_(pinned[k], non_blocking=True)
+            step(dst)
+            loss_host.copy_(loss, non_blocking=True)
+            stream.synchronize()
+        barrier()
+        e2e_s = (time.perf_counter() - t0) / n_e2e
+        if dist is not None:
+            tt = torch.tensor([e2e_s], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            e2e_s = float(tt.item())
+        e2e = dict(value=world * T / e2e_s, unit="tokens/s", h2d_bytes_per_step=int(h2d), d2h_bytes_per_step=4,
+                   ms_per_step=1e3 * e2e_s, steps=n_e2e)
+        del dst, pinned
+
+    # ---- CPU baseline: the oracle on a bounded sample, rank 0 at N = 1 only
+    cpu = None
+    if not args.no_cpu and world == 1 and rank == 0:
+        rate, secs = cpu_oracle_rate(cfg, h["W"].view(torch.int16).numpy().view(np.uint16)
+                                     if tdt == torch.bfloat16 else h["W"].numpy(), args.cpu_rows)
+        cpu = dict(value=rate, unit="tokens/s", cores=len(os.sched_getaffinity(0)), kind="oracle",
+                   sample=f"oracle fwd+bwd (fp64, full-vocab logit rows, analytic dH/dW) on rows 0..{args.cpu_rows - 1}"
+                          f" of {cfg.name}; {secs:.1f} s")
+
+    if rank == 0:
+        line = dict(metric=METRIC, value=tokens_per_s, unit="tokens/s", n_gpus=world, steps=args.steps,
+                    warmup=args.warmup, ms_per_step=1e3 * sec_per_step, higher_is_better=True, scaling="weak",
+                    vs_baseline=None, dtype=cfg.dtype, data="synthetic",
+                    config=dict(workload=cfg.name, T=T, d=d, V=V, K=K, tau=cfg.tau, chunk=chunk, valid_rows=n_valid,
+                                batch=cfg.batch, seq_len=cfg.seq_len or T,
+                                l2="inputs larger than L2 (H %.2f GB, W %.2f GB)" % (T * d * 2 / 1e9, V * d * 2 / 1e9),
+                                parallelism=f"replicas x{world}"),
+                    tflops=tflops, frac_bf16_peak=tflops / peak_burst,
+                    frac_bf16_peak_sustained=tflops / peak_sust, peak_source=peaks["source"],
+                    peak_device_gib=peak_alloc / 2 ** 30, nontorch_device_gib=max(0.0, (free0 - free1 - peak_alloc) / 2 ** 30),
+                    loss=loss_val, roofline=roofline, cpu_baseline=cpu, e2e=e2e, gpu_launches=int(launches),
+                    clocks=clk.summary())
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def _kernel_src_sha():
+    import hashlib
+
+    h = hashlib.sha256()
+    for f in ("fckl_tc.cu", "fckl_ptx.cuh", "fckl_api.cu"):
+        h.update(open(os.path.join(ROOT, "chunked_kl_loss_head_b300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+if __name__ == "__main__":
+    main()
