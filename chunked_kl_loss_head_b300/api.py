@@ -98,6 +98,17 @@ def fckl_backward(H, W, topk_idx, topk_logits, valid, tau, chunk, lse, grad_loss
     _check(st, "fckl_backward")
 
 
+def fckl_forward_noalloc(H, W, topk_idx, topk_logits, valid, tau, chunk, loss, lse, row_loss, status=None,
+                         stream=None):
+    """fckl_forward for callers that cannot allocate device memory: no workspace, the
+    library's own fixed scratch instead; row_loss is required, status optional."""
+    T, d, V, K = _shapes(H, W, topk_idx, topk_logits, valid)
+    st = lib().fckl_forward_noalloc(_ptr(H), _ptr(W), _ptr(topk_idx), _ptr(topk_logits), _ptr(valid), T, d, V, K,
+                                    float(tau), int(chunk), _dtype_code(H), _ptr(loss), _ptr(lse), _ptr(row_loss),
+                                    _ptr(status), _stream(stream))
+    _check(st, "fckl_forward_noalloc")
+
+
 def fckl_get_error(ws, stream=None) -> int:
     return int(lib().fckl_get_error(_ptr(ws), _stream(stream)))
 

@@ -154,6 +154,41 @@ FCKL_API fckl_status fckl_profile_read(int32_t kernel_class, int64_t* launches, 
 FCKL_API fckl_status fckl_debug_gemm_bf16(const void* A, const void* B, float* D, int64_t M, int64_t N,
                                  int64_t K, int32_t a_mn, int32_t b_mn, void* stream);
 
+/* ---- forward without a workspace --------------------------------------------------------
+ * The pages describe no such call: it has no counterpart in the method and exists only for
+ * callers of this library that cannot allocate device memory.  Such callers include code
+ * running while a CUDA stream is being captured into a graph (cudaMalloc is refused during
+ * capture), runtimes that reserve all device memory up front for their own pool and hand
+ * library code nothing but the buffers they own (a foreign cudaMalloc then fails), and
+ * latency-critical loops that cannot risk the device-wide synchronization cudaMalloc and
+ * cudaFree may cause.
+ *
+ * Size of the scratch array fckl_forward_noalloc keeps in the library's own device memory.
+ * Every GPU that loads the library holds this much until the process exits. */
+#define FCKL_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/* fckl_forward with the same arguments and results, except that it takes no workspace and
+ * allocates nothing (no cudaMalloc, cudaFree or allocating library routine).  Its scratch
+ * is a fixed FCKL_NOALLOC_SCRATCH_BYTES array in the library's device memory, so it needs
+ * the per-row loss output and an optional status output from the caller:
+ *   row_loss  device float32 [T], required when T > 0 (loss_t, 0 for ignored rows)
+ *   status    device int32 scalar or NULL; receives the status word of this call
+ *             (FCKL_OK, FCKL_ERR_BAD_INDEX or FCKL_ERR_TIMEOUT) once the work is done
+ * Rows are processed in chunks of at most `chunk` rows, smaller when a chunk's scratch
+ * (16*K + 8*ceil(V/256) bytes per row) would not fit; the results do not depend on the
+ * chunk size.  Returns FCKL_ERR_WORKSPACE when a single row's scratch exceeds
+ * FCKL_NOALLOC_SCRATCH_BYTES, before anything is launched.
+ * The first call on a device looks up the array's device address (and may load the
+ * library's GPU code); make that first call before any stream capture.  All calls share
+ * the one array, which keeps the last call's contents: the call clears what must start at
+ * zero itself, but calls that overlap on the GPU (other streams or host threads on the
+ * same device) race on it and must be serialized by the caller. */
+FCKL_API fckl_status fckl_forward_noalloc(const void* H, const void* W, const int32_t* topk_idx,
+                                          const float* topk_logits, const uint8_t* valid, int64_t T,
+                                          int64_t d, int64_t V, int32_t K, float tau, int64_t chunk,
+                                          fckl_dtype dtype, float* loss, float* lse, float* row_loss,
+                                          int32_t* status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
