@@ -271,11 +271,13 @@ def main():
     def class_flops(c):
         if c == "fwd_tiles":
             return 2.0 * d * V * T * args.steps
-        if c in ("bwd_tiles", "dW", "dH"):
+        if c == "bwd_tiles":
             return 2.0 * d * V * n_valid * args.steps
+        if c == "grad_gemm":
+            return 4.0 * d * V * n_valid * args.steps
         return 0.0
 
-    tc_classes = [c for c in ("fwd_tiles", "bwd_tiles", "dW", "dH") if per_class[c][0] > 0]
+    tc_classes = [c for c in ("fwd_tiles", "bwd_tiles", "grad_gemm") if per_class[c][0] > 0]
     total_ms = sum(v[1] for v in per_class.values())
     dom = max(tc_classes, key=lambda c: per_class[c][1])
     dom_launches, dom_ms = per_class[dom]

@@ -17,7 +17,7 @@ from ._lib import lib
 F32, BF16 = 0, 1
 STATUS = {0: "FCKL_OK", 1: "FCKL_ERR_INVALID_ARG", 2: "FCKL_ERR_UNSUPPORTED", 3: "FCKL_ERR_WORKSPACE",
           4: "FCKL_ERR_CUDA", 5: "FCKL_ERR_BAD_INDEX", 6: "FCKL_ERR_TIMEOUT"}
-KERNEL_CLASSES = ["prep", "fwd_tiles", "combine", "reduce", "bwd_tiles", "dW", "dH", "other"]
+KERNEL_CLASSES = ["prep", "fwd_tiles", "combine", "reduce", "bwd_tiles", "grad_gemm", "other"]
 
 
 class FcklError(RuntimeError):

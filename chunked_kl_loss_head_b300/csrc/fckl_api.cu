@@ -39,7 +39,8 @@ int64_t stripe_width(int64_t C, int64_t V, size_t g_elem) {
 }
 
 struct Layout {
-  size_t ctrl, row_loss, sidx, sp, slogp, zk, part, G, dHacc, total;
+  size_t ctrl, row_loss, sidx, sp, slogp, zk, part, G, dHacc, HcT, total;
+  int64_t ldT;
 };
 
 Layout layout_of(const Sizes& z) {
@@ -60,6 +61,8 @@ Layout layout_of(const Sizes& z) {
   L.part = take(8 * static_cast<size_t>(z.C) * static_cast<size_t>(z.nvt));
   L.G = take(static_cast<size_t>(z.C) * static_cast<size_t>(z.S) * (z.elem == 2 ? 2 : 4));
   L.dHacc = take(z.elem == 2 ? 4 * static_cast<size_t>(z.C) * static_cast<size_t>(z.d) : 0);
+  L.ldT = (z.C + 7) / 8 * 8;
+  L.HcT = take(z.elem == 2 ? 2 * static_cast<size_t>(z.d) * static_cast<size_t>(L.ldT) : 0);
   L.total = off;
   return L;
 }
@@ -120,6 +123,8 @@ ChunkScratch scratch_of(void* ws, const Layout& L) {
   s.part = reinterpret_cast<float2*>(b + L.part);
   s.G = b + L.G;
   s.dHacc = reinterpret_cast<float*>(b + L.dHacc);
+  s.HcT = b + L.HcT;
+  s.ldT = L.ldT;
   return s;
 }
 
@@ -199,8 +204,8 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-bool encode_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
-                         uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer) {
+static bool encode_2d(CUtensorMapDataType dt, CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                      uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {inner, outer};
@@ -208,10 +213,19 @@ bool encode_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uin
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t es[2] = {1, 1};
   std::memset(map, 0, sizeof(*map));
-  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+bool encode_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                         uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer) {
+  return encode_2d(CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, map, base, inner, outer, row_stride_bytes, box_inner, box_outer);
+}
+
+bool encode_tmap_f32_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                        uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer) {
+  return encode_2d(CU_TENSOR_MAP_DATA_TYPE_FLOAT32, map, base, inner, outer, row_stride_bytes, box_inner, box_outer);
 }
 
 }  // namespace fckl
@@ -243,6 +257,7 @@ fckl_status fckl_forward(const void* H, const void* W, const int32_t* topk_idx, 
   ChunkScratch s = scratch_of(ws, L);
 
   FCKL_TRY(step(FCKL_K_OTHER, st, [&] { return cudaMemsetAsync(ctrl, 0, sizeof(Ctrl), st); }));
+  TileSched sched{&ctrl->tile_counter, 0};
   const int nvt = static_cast<int>(z.nvt);
   for (int64_t c0 = 0; c0 < T; c0 += z.C) {
     const int64_t rows = (T - c0 < z.C) ? T - c0 : z.C;
@@ -252,7 +267,7 @@ fckl_status fckl_forward(const void* H, const void* W, const int32_t* topk_idx, 
     if (dtype == FCKL_BF16) {
       const void* Hc = static_cast<const uint8_t*>(H) + c0 * d * 2;
       FCKL_TRY(step(FCKL_K_FWD_TILES, st, [&] {
-        return tc_fwd_tiles(Hc, W, rows, d, V, tau, s.sidx, K, s.zk, s.part, nvt, ctrl, num_sms, st);
+        return tc_fwd_tiles(Hc, W, rows, d, V, tau, s.sidx, K, s.zk, s.part, nvt, ctrl, &sched, num_sms, st);
       }));
     } else {
       const float* Hc = static_cast<const float*>(H) + c0 * d;
@@ -290,6 +305,9 @@ fckl_status fckl_backward(const void* H, const void* W, const int32_t* topk_idx,
   if (T == 0) {
     return step(FCKL_K_OTHER, st, [&] { return cudaMemsetAsync(dW, 0, sizeof(float) * V * d, st); });
   }
+  FCKL_TRY(step(FCKL_K_OTHER, st,
+                [&] { return cudaMemsetAsync(&ctrl->tile_counter, 0, sizeof(ctrl->tile_counter), st); }));
+  TileSched sched{&ctrl->tile_counter, 0};
   FCKL_TRY(step(FCKL_K_REDUCE, st, [&] { return launch_grad_scale(valid, T, tau, grad_loss, grad_scale, ctrl, st); }));
   const int64_t S = z.S;
   for (int64_t c0 = 0; c0 < T; c0 += z.C) {
@@ -297,6 +315,10 @@ fckl_status fckl_backward(const void* H, const void* W, const int32_t* topk_idx,
     FCKL_TRY(step(FCKL_K_PREP, st, [&] {
       return launch_prep(topk_idx + c0 * K, topk_logits + c0 * K, rows, K, V, tau, s, ctrl, st);
     }));
+    if (dtype == FCKL_BF16) {
+      const void* Hc = static_cast<const uint8_t*>(H) + c0 * d * 2;
+      FCKL_TRY(step(FCKL_K_OTHER, st, [&] { return launch_transpose_bf16(Hc, rows, d, d, s.HcT, s.ldT, st); }));
+    }
     for (int64_t s0 = 0; s0 < V; s0 += S) {
       const int64_t s_eff = (V - s0 < S) ? V - s0 : S;
       const bool last = s0 + S >= V;
@@ -305,15 +327,16 @@ fckl_status fckl_backward(const void* H, const void* W, const int32_t* topk_idx,
         const void* Ws = static_cast<const uint8_t*>(W) + s0 * d * 2;
         FCKL_TRY(step(FCKL_K_BWD_TILES, st, [&] {
           return tc_bwd_tiles(Hc, W, rows, d, V, s0, S, tau, s.sidx, s.sp, K, lse + c0, valid + c0, ctrl, s.G, S,
-                              num_sms, st);
+                              &sched, num_sms, st);
         }));
-        FCKL_TRY(step(FCKL_K_DW, st, [&] {
-          return tc_dW(s.G, S, Hc, rows, d, s_eff, dW + s0 * d, c0 > 0, ctrl, num_sms, st);
+        FCKL_TRY(step(FCKL_K_GRAD_GEMM, st, [&] {
+          return tc_dW_dH(s.G, S, s.HcT, s.ldT, Ws, rows, d, s_eff, dW + s0 * d, c0 > 0, s.dHacc, s0 > 0, ctrl, &sched,
+                          num_sms, st);
         }));
-        void* out = last ? static_cast<uint8_t*>(dH) + c0 * d * 2 : nullptr;
-        FCKL_TRY(step(FCKL_K_DH, st, [&] {
-          return tc_dH(s.G, S, Ws, rows, d, s_eff, s.dHacc, s0 > 0, out, ctrl, num_sms, st);
-        }));
+        if (last) {
+          void* out = static_cast<uint8_t*>(dH) + c0 * d * 2;
+          FCKL_TRY(step(FCKL_K_OTHER, st, [&] { return launch_f32_to_bf16(s.dHacc, out, rows * d, st); }));
+        }
       } else {
         const float* Hc = static_cast<const float*>(H) + c0 * d;
         const float* Wf = static_cast<const float*>(W);
@@ -322,11 +345,11 @@ fckl_status fckl_backward(const void* H, const void* W, const int32_t* topk_idx,
           return launch_simt_bwd_tiles(Hc, Wf, rows, d, V, s0, S, tau, s.sidx, s.sp, K, lse + c0, valid + c0, ctrl, G,
                                        st);
         }));
-        FCKL_TRY(step(FCKL_K_DW, st, [&] {
+        FCKL_TRY(step(FCKL_K_GRAD_GEMM, st, [&] {
           return launch_simt_gemm(G, 1, S, Hc, d, 1, dW + s0 * d, d, s_eff, d, rows, c0 > 0, st);
         }));
         float* dHc = static_cast<float*>(dH) + c0 * d;
-        FCKL_TRY(step(FCKL_K_DH, st, [&] {
+        FCKL_TRY(step(FCKL_K_GRAD_GEMM, st, [&] {
           return launch_simt_gemm(G, S, 1, Wf + s0 * d, d, 1, dHc, d, rows, d, s_eff, s0 > 0, st);
         }));
       }

@@ -22,6 +22,15 @@ struct Ctrl {
   float grad_alpha;      // g / (tau * N) for the backward (0 when N = 0)
   float pad1;
   double loss_sum;       // sum of valid loss_t of the last forward
+  uint32_t tile_counter; // dynamic tile scheduler of the tensor-core launches
+  uint32_t pad2;
+};
+
+// Host-side view of the tile counter: its device address and the value it will hold when
+// the next launch on the stream starts.
+struct TileSched {
+  unsigned int* counter;
+  unsigned int value;
 };
 
 // Records `code` as the workspace status unless one is already recorded.
@@ -38,6 +47,8 @@ struct ChunkScratch {
   float2* part;     // [C, nvt] per (row, 256-wide vocab tile): (max, sum) in log2 units
   void* G;          // [C, S] gradient tile stripe (bf16 for bf16 work, f32 for f32 work)
   float* dHacc;     // [C, d] fp32 dH accumulator (bf16 work only)
+  void* HcT;        // [d, ldT] bf16 transposed hidden states of the chunk (bf16 work only)
+  int64_t ldT;      // C rounded up to a multiple of 8
 };
 
 // ---- row kernels (fckl_rowops.cu) --------------------------------------------------------
@@ -51,6 +62,9 @@ cudaError_t launch_loss_reduce(const float* row_loss, const uint8_t* valid, int6
 cudaError_t launch_grad_scale(const uint8_t* valid, int64_t T, float tau, float grad_loss,
                               const float* grad_scale, Ctrl* ctrl, cudaStream_t st);
 cudaError_t launch_f32_to_bf16(const float* src, void* dst, int64_t n, cudaStream_t st);
+// out[c, r] = in[r, c] for bf16 in[rows, cols] (row stride ld_in) -> out[cols, ld_out]
+cudaError_t launch_transpose_bf16(const void* in, int64_t rows, int64_t cols, int64_t ld_in, void* out,
+                                  int64_t ld_out, cudaStream_t st);
 
 // ---- fp32 CUDA-core path (fckl_simt.cu) --------------------------------------------------
 cudaError_t launch_simt_fwd_tiles(const float* Hc, const float* W, int64_t rows, int64_t d, int64_t V,
@@ -68,25 +82,27 @@ cudaError_t launch_simt_gemm(const float* A, int64_t sam, int64_t sak, const flo
 // ---- bf16 tensor-core path (fckl_tc.cu) --------------------------------------------------
 cudaError_t tc_fwd_tiles(const void* Hc, const void* W, int64_t rows, int64_t d, int64_t V,
                          float tau, const int32_t* sidx, int32_t K, float* zk, float2* part, int nvt,
-                         Ctrl* ctrl, int num_sms, cudaStream_t st);
+                         Ctrl* ctrl, TileSched* sched, int num_sms, cudaStream_t st);
 cudaError_t tc_bwd_tiles(const void* Hc, const void* W, int64_t rows, int64_t d, int64_t V,
                          int64_t s0, int64_t S, float tau, const int32_t* sidx, const float* sp,
                          int32_t K, const float* lse, const uint8_t* valid, Ctrl* ctrl,
-                         void* G, int64_t ldG, int num_sms, cudaStream_t st);
-// dW[s0:s0+S, :] (+)= G^T . Hc    (G is [rows, ldG] bf16, first S columns used)
-cudaError_t tc_dW(const void* G, int64_t ldG, const void* Hc, int64_t rows, int64_t d, int64_t S,
-                  float* dW_stripe, int accumulate, Ctrl* ctrl, int num_sms, cudaStream_t st);
-// dH accumulator: acc[rows, d] (+)= G . W[s0:s0+S, :]; when `out_bf16` is non-null the final
-// sum is written there as bf16 instead of back to acc.
-cudaError_t tc_dH(const void* G, int64_t ldG, const void* W_stripe, int64_t rows, int64_t d,
-                  int64_t S, float* acc, int accumulate, void* out_bf16, Ctrl* ctrl, int num_sms,
-                  cudaStream_t st);
+                         void* G, int64_t ldG, TileSched* sched, int num_sms, cudaStream_t st);
+// One launch for both contractions of a (chunk, stripe) step, G being [rows, ldG] bf16 with
+// its first S columns used and HcT the chunk's hidden states transposed, [d, ldT] bf16:
+//   dH accumulator acc[rows, d] (+)= G . W[s0:s0+S, :]
+//   dW[s0:s0+S, :] (+)= G^T . Hc
+cudaError_t tc_dW_dH(const void* G, int64_t ldG, const void* HcT, int64_t ldT, const void* W_stripe,
+                     int64_t rows, int64_t d, int64_t S, float* dW_stripe, int dW_accumulate,
+                     float* dH_acc, int dH_accumulate, Ctrl* ctrl, TileSched* sched, int num_sms,
+                     cudaStream_t st);
 cudaError_t tc_debug_gemm(const void* A, const void* B, float* D, int64_t M, int64_t N, int64_t K,
                           int a_mn, int b_mn, int num_sms, cudaStream_t st);
 
 // ---- host helpers (fckl_api.cu) ----------------------------------------------------------
 bool encode_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                          uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer);
+bool encode_tmap_f32_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                        uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer);
 void count_launch(fckl_kernel_class cls);
 void prof_begin(fckl_kernel_class cls, cudaStream_t st);
 void prof_end(fckl_kernel_class cls, cudaStream_t st);

@@ -105,6 +105,7 @@ extern "C" fckl_status fckl_forward_noalloc(const void* H, const void* W, const 
 
   // the previous call's status word must not leak into this one
   if (cudaMemsetAsync(ctrl, 0, sizeof(Ctrl), st) != cudaSuccess) return FCKL_ERR_CUDA;
+  TileSched sched{&ctrl->tile_counter, 0};
   const int nv = static_cast<int>(nvt);
   for (int64_t c0 = 0; c0 < T; c0 += rows_max) {
     const int64_t rows = (T - c0 < rows_max) ? T - c0 : rows_max;
@@ -114,7 +115,7 @@ extern "C" fckl_status fckl_forward_noalloc(const void* H, const void* W, const 
     cudaError_t e;
     if (dtype == FCKL_BF16) {
       e = tc_fwd_tiles(static_cast<const uint8_t*>(H) + c0 * d * 2, W, rows, d, V, tau, s.sidx, K, s.zk, s.part, nv,
-                       ctrl, num_sms, st);
+                       ctrl, &sched, num_sms, st);
     } else {
       e = launch_simt_fwd_tiles(static_cast<const float*>(H) + c0 * d, static_cast<const float*>(W), rows, d, V, tau,
                                 s.sidx, K, s.zk, s.part, nv, st);

@@ -177,7 +177,32 @@ __global__ void f32_to_bf16_kernel(const float4* __restrict__ src, __nv_bfloat16
   }
 }
 
+// Tiled transpose of a bf16 matrix through shared memory (32 x 32 tiles, coalesced on
+// both sides).
+__global__ void transpose_bf16_kernel(const uint16_t* __restrict__ in, int64_t rows, int64_t cols, int64_t ld_in,
+                                      uint16_t* __restrict__ out, int64_t ld_out) {
+  __shared__ uint16_t tile[32][33];
+  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * 32, r0 = static_cast<int64_t>(blockIdx.y) * 32;
+  for (int j = threadIdx.y; j < 32; j += 8) {
+    const int64_t r = r0 + j, c = c0 + threadIdx.x;
+    if (r < rows && c < cols) tile[j][threadIdx.x] = in[r * ld_in + c];
+  }
+  __syncthreads();
+  for (int j = threadIdx.y; j < 32; j += 8) {
+    const int64_t c = c0 + j, r = r0 + threadIdx.x;
+    if (r < rows && c < cols) out[c * ld_out + r] = tile[threadIdx.x][j];
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_transpose_bf16(const void* in, int64_t rows, int64_t cols, int64_t ld_in, void* out, int64_t ld_out,
+                                  cudaStream_t st) {
+  const dim3 grid(static_cast<unsigned>((cols + 31) / 32), static_cast<unsigned>((rows + 31) / 32));
+  transpose_bf16_kernel<<<grid, dim3(32, 8), 0, st>>>(static_cast<const uint16_t*>(in), rows, cols, ld_in,
+                                                      static_cast<uint16_t*>(out), ld_out);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_prep(const int32_t* idx, const float* logits, int64_t rows, int32_t K, int64_t V,
                         float tau, ChunkScratch s, Ctrl* ctrl, cudaStream_t st) {

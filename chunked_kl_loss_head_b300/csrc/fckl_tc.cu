@@ -1,9 +1,10 @@
 // fckl_tc.cu -- the bf16 path on 5th-generation tensor cores (tcgen05) for sm_103a.
 //
 // One persistent, warp-specialized GEMM engine serves every contraction of the loss:
-//   warp 0      TMA producer: streams 64-deep K slabs of A and B into a ring of shared-
-//               memory stages (128-byte swizzle), completion tracked by mbarriers;
-//   warp 1      MMA issuer: one thread issues tcgen05.mma (M=128, N=BN, K=16 per
+//   warp 0      TMA producer: hands out tiles and streams 64-deep K slabs of A and B
+//               into a ring of shared-memory stages (128-byte swizzle), completion
+//               tracked by mbarriers;
+//   warp 1      MMA issuer: one thread issues tcgen05.mma (M=128, N=bn, K=16 per
 //               instruction) into one of two TMEM accumulators and commits each stage
 //               back to the producer when the tensor core has read it;
 //   warps 2-5   epilogue: tcgen05.ld of the finished accumulator, one tile row per
@@ -12,7 +13,8 @@
 //   FwdEpi   logit tile -> running max / sum of exp per row + student logits at the
 //            teacher ids (the tile is never written out);
 //   BwdEpi   recomputed logit tile -> G = (softmax - p_teacher) * g / (tau N) in bf16;
-//   F32Epi   plain fp32 store / accumulate (dW, dH and the engine's test hook).
+//   F32Epi   fp32 tile -> TMA store or TMA reduce-add (dW, dH and the engine's test hook),
+//            optionally transposed.
 #include <cuda_bf16.h>
 
 #include <atomic>
@@ -27,26 +29,74 @@ namespace fckl {
 namespace {
 
 constexpr int BM = 128;
-constexpr int BK = 64;           // one 128-byte swizzle row of bf16
-constexpr int kThreads = 192;    // 6 warps
-constexpr int kEpiThreads = 128; // warps 2..5
-constexpr int kTmemCols = 512;   // two accumulators of up to 256 fp32 columns
+constexpr int BK = 64;            // one 128-byte swizzle row of bf16
+constexpr int kBNMax = 256;       // widest tile (N) of any problem
+constexpr int kThreads = 192;     // 6 warps
+constexpr int kEpiThreads = 128;  // warps 2..5
+constexpr int kTmemCols = 512;    // two accumulators of up to 256 fp32 columns
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kSmemBudget = 220 * 1024;
+constexpr int kSmemMax = 232448;  // opt-in dynamic shared memory per block
 
-template <int BN>
+template <int STAGING>
 struct Shape {
   static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int B_BYTES = kBNMax * BK * 2;
   static constexpr int STAGE = A_BYTES + B_BYTES;
-  static constexpr int STAGES = (kSmemBudget / STAGE) > 8 ? 8 : (kSmemBudget / STAGE);
-  static constexpr int BAR_BYTES = 256;
-  static constexpr int SMEM = 1024 + STAGES * STAGE + BAR_BYTES;
+  static constexpr int BAR_BYTES = 512;
+  static constexpr int FIT = (kSmemMax - 1024 - BAR_BYTES - STAGING) / STAGE;
+  static constexpr int STAGES = FIT > 8 ? 8 : FIT;
+  static constexpr int SMEM = 1024 + STAGES * STAGE + STAGING + BAR_BYTES;
 };
 
-struct Geom {
-  int num_m, num_n, num_k;
+// What the engine hands every epilogue besides its TMEM address: the output tensor map
+// of the tile's problem (TMA epilogues) and this CTA's staging shared memory.
+struct EpiCtx {
+  const CUtensorMap* out;
+  uint8_t* staging;
 };
+
+// One GEMM problem of a launch: D[M, N] = A . B over K, tiled 128 x bn x 64.
+struct Prob {
+  int num_m, num_n, num_k;
+  int tiles;       // num_m * num_n
+  int a_mn, b_mn;  // operand layouts (see the engine)
+  int n_fastest;   // raster: consecutive tiles walk N (1) or M (0)
+  int bn;          // tile width: a multiple of 32 (of 64 for an MN-major B), at most 256
+};
+
+// A launch: one or two problems (tiles of the second follow those of the first), and the
+// dynamic tile counter (a word in the workspace that reads `base` when the launch starts),
+// or none for static round-robin scheduling.
+struct Geom {
+  Prob p[2];
+  int nprob;
+  int tiles;
+  unsigned int* counter;
+  unsigned int base;
+};
+
+struct TileRef {
+  int prob, m_t, n_t;
+};
+
+__device__ __forceinline__ TileRef tile_of(const Geom& g, int t) {
+  int p = 0;
+  if (g.nprob > 1 && t >= g.p[0].tiles) {
+    t -= g.p[0].tiles;
+    p = 1;
+  }
+  const Prob q = p ? g.p[1] : g.p[0];
+  TileRef r;
+  r.prob = p;
+  if (q.n_fastest) {
+    r.n_t = t % q.num_n;
+    r.m_t = t / q.num_n;
+  } else {
+    r.m_t = t % q.num_m;
+    r.n_t = t / q.num_m;
+  }
+  return r;
+}
 
 // Shared flag: a role that gave up on a wait tells the others to stop waiting.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
@@ -101,8 +151,10 @@ struct FwdEpi {
   int nvt;
   Ctrl* ctrl;
 
-  template <int BN>
-  __device__ __forceinline__ void run(uint32_t taddr, int m_t, int n_t, int r) const {
+  static constexpr int kStaging = 0;
+
+  __device__ __forceinline__ void run(uint32_t taddr, int m_t, int n_t, int r, int BN, const EpiCtx&,
+                                      uint32_t&) const {
     const int64_t row = static_cast<int64_t>(m_t) * BM + r;
     const bool live = row < rows;
     const int64_t n0 = static_cast<int64_t>(n_t) * BN;
@@ -154,8 +206,10 @@ struct BwdEpi {
   Ctrl* ctrl;
   __nv_bfloat16* G;
 
-  template <int BN>
-  __device__ __forceinline__ void run(uint32_t taddr, int m_t, int n_t, int r) const {
+  static constexpr int kStaging = 0;
+
+  __device__ __forceinline__ void run(uint32_t taddr, int m_t, int n_t, int r, int BN, const EpiCtx&,
+                                      uint32_t&) const {
     const int64_t row = static_cast<int64_t>(m_t) * BM + r;
     const bool live = row < rows;
     const int64_t n0l = static_cast<int64_t>(n_t) * BN;
@@ -203,76 +257,103 @@ struct BwdEpi {
   }
 };
 
-// fp32 result tile: out[row, col] = acc (+ out when accumulate); with out_bf16 set, the
-// (accumulated) value goes to out_bf16 as bf16 instead.  N and ldo are multiples of 4.
+// fp32 result tile through TMA.  Each epilogue warp owns 32 rows of the tile; per
+// 32-column chunk it writes a 32 x 32 fp32 block into one of its two 4 KB staging buffers
+// (128-byte swizzle: rows of 128 bytes whose 16-byte pieces are permuted by row % 8, so a
+// warp's stores hit distinct banks) and one lane issues a TMA reduce-add into the output
+// (accumulate) or a TMA store (first pass).  The read-modify-write happens in L2 and the
+// epilogue never waits on HBM.  With `transpose`, D[m, n] goes to out[n][m]: the block is
+// written transposed into the buffer and stored at (x = m, y = n).  The output map has a
+// 32 x 32 box and clips everything outside the M x N result.
 struct F32Epi {
-  float* out;
-  int64_t ldo, M, N;
-  int accumulate;
-  __nv_bfloat16* out_bf16;
+  int64_t M, N;  // of D
+  int accumulate, transpose;
   Ctrl* ctrl;
 
-  template <int BN>
-  __device__ __forceinline__ void run(uint32_t taddr, int m_t, int n_t, int r) const {
-    const int64_t row = static_cast<int64_t>(m_t) * BM + r;
-    const bool live = row < M;
-    const int64_t n0 = static_cast<int64_t>(n_t) * BN;
+  static constexpr int kWarpStaging = 2 * 32 * 32 * 4;
+  static constexpr int kStaging = 4 * kWarpStaging;
+
+  __device__ __forceinline__ void run(uint32_t taddr, int m_t, int n_t, int r, int bn, const EpiCtx& cx,
+                                      uint32_t& seq) const {
+    const int lane = r & 31, quad = r >> 5;
+    uint8_t* wbuf = cx.staging + quad * kWarpStaging;
+    const int64_t n0 = static_cast<int64_t>(n_t) * bn;
+    const int64_t m0 = static_cast<int64_t>(m_t) * BM + quad * 32;
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 32) {
+    for (int c = 0; c < bn; c += 32) {
       if (n0 + c >= N) break;
+      uint8_t* buf = wbuf + (seq & 1) * (32 * 32 * 4);
+      ++seq;
+      if (lane == 0) bulk_wait_read<1>();  // the copy issued two chunks ago has read `buf`
+      __syncwarp();
       uint32_t v[32];
       tmem_ld_32x32(taddr + c, v);
       tmem_ld_wait();
-      if (!live) continue;
-      float* o = out + row * ldo + n0 + c;
+      if (!transpose) {
+        uint8_t* rowp = buf + lane * 128;
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        if (n0 + c + 4 * q >= N) break;
-        float4 x = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                               __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
-        if (accumulate) {
-          const float4 y = *reinterpret_cast<const float4*>(o + 4 * q);
-          x.x += y.x;
-          x.y += y.y;
-          x.z += y.z;
-          x.w += y.w;
+        for (int q = 0; q < 8; ++q) {
+          const uint4 x = make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+          *reinterpret_cast<uint4*>(rowp + ((q ^ (lane & 7)) << 4)) = x;
         }
-        if (out_bf16) {
-          __nv_bfloat162 lo = __floats2bfloat162_rn(x.x, x.y), hi = __floats2bfloat162_rn(x.z, x.w);
-          uint2 pk = make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
-          *reinterpret_cast<uint2*>(out_bf16 + row * ldo + n0 + c + 4 * q) = pk;
-        } else {
-          *reinterpret_cast<float4*>(o + 4 * q) = x;
-        }
+      } else {
+        const int piece = lane >> 2, word = (lane & 3) << 2;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          *reinterpret_cast<uint32_t*>(buf + j * 128 + ((piece ^ (j & 7)) << 4) + word) = v[j];
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0 && m0 < M) {
+        const int32_t x = static_cast<int32_t>(transpose ? m0 : n0 + c);
+        const int32_t y = static_cast<int32_t>(transpose ? n0 + c : m0);
+        if (accumulate) tma_reduce_add_2d(cx.out, buf, x, y);
+        else tma_store_2d(cx.out, buf, x, y);
+        bulk_commit();
       }
     }
   }
 };
 
 // ----------------------------------------------------------------------------------------
-// The engine.  A_MN / B_MN select the operand layouts:
+// The engine.  Per problem, a_mn / b_mn select the operand layouts:
 //   A K-major: A[m, k] at row m of a [M, K] tensor (TMA box 64 x 128);
 //   A MN-major: A[m, k] at row k of a [K, M] tensor (two 64 x 64 boxes per stage);
-//   B K-major: B[n, k] at row n of a [N, K] tensor (box 64 x BN), so D = A . B^T;
-//   B MN-major: B[k, n] at row k of a [K, N] tensor (BN/64 boxes of 64 x 64).
-template <int BN, bool A_MN, bool B_MN, class Epi>
+//   B K-major: B[n, k] at row n of a [N, K] tensor (box 64 x bn), so D = A . B^T;
+//   B MN-major: B[k, n] at row k of a [K, N] tensor (bn/64 boxes of 64 x 64).
+// (On this part an MN-major B operand costs 12-25% of MMA throughput and an MN-major A
+// nothing, so the loss arranges its contractions to have K-major B operands.)
+// Tiles are handed out by the producer warp: from the global counter when there is one
+// (each CTA takes the next tile when it is ready for one, which balances tiles of
+// different cost), else round-robin; the tile sequence reaches the MMA warp and the
+// epilogue warps through a small shared-memory queue.
+constexpr int kQueue = 4;
+
+template <class Epi>
 __global__ void __launch_bounds__(kThreads, 1)
-    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, Geom g,
-                   Epi epi) {
-  using S = Shape<BN>;
-  constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, A_MN, B_MN);
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmB0,
+                   const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
+                   const __grid_constant__ CUtensorMap tmO0, const __grid_constant__ CUtensorMap tmO1, Geom g,
+                   Epi e0, Epi e1) {
+  using S = Shape<Epi::kStaging>;
+  constexpr uint32_t IDESC = idesc_bf16_f32(BM, 8, false, false) & ~(0x3Fu << 17);  // N filled per problem
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + S::STAGES * S::A_BYTES;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sB + S::STAGES * S::B_BYTES);
+  uint8_t* staging = sB + S::STAGES * S::B_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(staging + Epi::kStaging);
   uint64_t* empty = full + S::STAGES;
   uint64_t* tfull = empty + S::STAGES;
   uint64_t* tempty = tfull + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  uint64_t* qfull = tempty + 2;
+  uint64_t* qempty = qfull + kQueue;
+  int* tileq = reinterpret_cast<int*>(qempty + kQueue);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tileq + kQueue);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  Ctrl* ctrl = e0.ctrl;
   if (threadIdx.x == 0) {
     for (int s = 0; s < S::STAGES; ++s) {
       mbar_init(&full[s], 1);
@@ -282,13 +363,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&tfull[a], 1);
       mbar_init(&tempty[a], kEpiThreads);
     }
+    for (int q = 0; q < kQueue; ++q) {
+      mbar_init(&qfull[q], 1);
+      mbar_init(&qempty[q], 1 + kEpiThreads);
+    }
     *abort_flag = 0;
     fence_mbar_init();
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    fence_proxy_async_smem();
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tmA);
-    tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmA0);
+    tma_prefetch_desc(&tmB0);
+    if (Epi::kStaging) tma_prefetch_desc(&tmO0);
+    if (g.nprob > 1) {
+      tma_prefetch_desc(&tmA1);
+      tma_prefetch_desc(&tmB1);
+      if (Epi::kStaging) tma_prefetch_desc(&tmO1);
+    }
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, kTmemCols);
@@ -298,50 +389,75 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int num_tiles = g.num_m * g.num_n;
-  Ctrl* ctrl = epi.ctrl;
 
   if (warp == 0) {
     if (lane == 0) {
       uint32_t it = 0;
-      bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-        const int m_t = tile % g.num_m, n_t = tile / g.num_m;
-        for (int kb = 0; kb < g.num_k; ++kb, ++it) {
+      int next_static = blockIdx.x;
+      for (int i = 0;; ++i) {
+        const int slot = i % kQueue;
+        if (!wait_or_abort(&qempty[slot], ((i / kQueue) & 1) ^ 1, abort_flag, ctrl)) break;
+        int t;
+        if (g.counter) {
+          t = static_cast<int>(atomicAdd(g.counter, 1u) - g.base);
+        } else {
+          t = next_static;
+          next_static += gridDim.x;
+        }
+        if (t >= g.tiles) t = -1;
+        tileq[slot] = t;
+        mbar_arrive(&qfull[slot]);
+        if (t < 0) break;
+        const TileRef tr = tile_of(g, t);
+        const Prob q = tr.prob ? g.p[1] : g.p[0];
+        const CUtensorMap* ta = tr.prob ? &tmA1 : &tmA0;
+        const CUtensorMap* tb = tr.prob ? &tmB1 : &tmB0;
+        const uint32_t tx = S::A_BYTES + static_cast<uint32_t>(q.bn) * BK * 2;
+        bool ok = true;
+        for (int kb = 0; kb < q.num_k; ++kb, ++it) {
           const int s = it % S::STAGES;
           const uint32_t ph = (it / S::STAGES) & 1;
           if (!wait_or_abort(&empty[s], ph ^ 1, abort_flag, ctrl)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[s], S::STAGE);
+          mbar_arrive_expect_tx(&full[s], tx);
           uint8_t* a = sA + s * S::A_BYTES;
           uint8_t* b = sB + s * S::B_BYTES;
-          if (!A_MN) {
-            tma_load_2d(a, &tmA, &full[s], kb * BK, m_t * BM);
+          if (!q.a_mn) {
+            tma_load_2d(a, ta, &full[s], kb * BK, tr.m_t * BM);
           } else {
-            tma_load_2d(a, &tmA, &full[s], m_t * BM, kb * BK);
-            tma_load_2d(a + 8192, &tmA, &full[s], m_t * BM + 64, kb * BK);
+            tma_load_2d(a, ta, &full[s], tr.m_t * BM, kb * BK);
+            tma_load_2d(a + 8192, ta, &full[s], tr.m_t * BM + 64, kb * BK);
           }
-          if (!B_MN) {
-            tma_load_2d(b, &tmB, &full[s], kb * BK, n_t * BN);
+          if (!q.b_mn) {
+            tma_load_2d(b, tb, &full[s], kb * BK, tr.n_t * q.bn);
           } else {
-#pragma unroll
-            for (int h = 0; h < BN / 64; ++h) tma_load_2d(b + h * 8192, &tmB, &full[s], n_t * BN + h * 64, kb * BK);
+            for (int h = 0; h < q.bn / 64; ++h) tma_load_2d(b + h * 8192, tb, &full[s], tr.n_t * q.bn + h * 64, kb * BK);
           }
         }
+        if (!ok) break;
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      uint32_t it = 0, lt = 0;
-      bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++lt) {
-        const uint32_t acc = lt & 1, use = lt >> 1;
+      uint32_t it = 0;
+      for (int i = 0;; ++i) {
+        const int slot = i % kQueue;
+        if (!wait_or_abort(&qfull[slot], (i / kQueue) & 1, abort_flag, ctrl)) break;
+        const int t = tileq[slot];
+        mbar_arrive(&qempty[slot]);
+        if (t < 0) break;
+        const TileRef tr = tile_of(g, t);
+        const Prob q = tr.prob ? g.p[1] : g.p[0];
+        const uint32_t idesc = IDESC | (static_cast<uint32_t>(q.bn >> 3) << 17) |
+                               (static_cast<uint32_t>(q.a_mn) << 15) | (static_cast<uint32_t>(q.b_mn) << 16);
+        const uint32_t acc = i & 1, use = i >> 1;
         if (!wait_or_abort(&tempty[acc], (use & 1) ^ 1, abort_flag, ctrl)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + acc * BN;
-        for (int kb = 0; kb < g.num_k; ++kb, ++it) {
+        const uint32_t d_tmem = tmem_base + acc * kBNMax;
+        bool ok = true;
+        for (int kb = 0; kb < q.num_k; ++kb, ++it) {
           const int s = it % S::STAGES;
           const uint32_t ph = (it / S::STAGES) & 1;
           if (!wait_or_abort(&full[s], ph, abort_flag, ctrl)) {
@@ -353,9 +469,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t b_base = smem_u32(sB + s * S::B_BYTES);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
-            const uint64_t ad = A_MN ? sdesc_sw128(a_base + k * 2048, 8192, 1024) : sdesc_sw128(a_base + k * 32, 16, 1024);
-            const uint64_t bd = B_MN ? sdesc_sw128(b_base + k * 2048, 8192, 1024) : sdesc_sw128(b_base + k * 32, 16, 1024);
-            umma_f16(d_tmem, ad, bd, IDESC, (kb | k) != 0);
+            const uint64_t ad =
+                q.a_mn ? sdesc_sw128(a_base + k * 2048, 8192, 1024) : sdesc_sw128(a_base + k * 32, 16, 1024);
+            const uint64_t bd =
+                q.b_mn ? sdesc_sw128(b_base + k * 2048, 8192, 1024) : sdesc_sw128(b_base + k * 32, 16, 1024);
+            umma_f16(d_tmem, ad, bd, idesc, (kb | k) != 0);
           }
           umma_commit(&empty[s]);
         }
@@ -366,16 +484,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     const int quad = warp & 3;  // TMEM lane quadrant this warp may access
     const int r = quad * 32 + lane;
-    uint32_t lt = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++lt) {
-      const int m_t = tile % g.num_m, n_t = tile / g.num_m;
-      const uint32_t acc = lt & 1, use = lt >> 1;
+    uint32_t seq = 0;  // staging-buffer sequence of this warp (TMA epilogues)
+    for (int i = 0;; ++i) {
+      const int slot = i % kQueue;
+      if (!wait_or_abort(&qfull[slot], (i / kQueue) & 1, abort_flag, ctrl)) break;
+      const int t = tileq[slot];
+      mbar_arrive(&qempty[slot]);
+      if (t < 0) break;
+      const TileRef tr = tile_of(g, t);
+      const uint32_t acc = i & 1, use = i >> 1;
       if (!wait_or_abort(&tfull[acc], use & 1, abort_flag, ctrl)) break;
       tc_fence_after();
-      epi.template run<BN>(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN, m_t, n_t, r);
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * kBNMax;
+      if (tr.prob) {
+        const EpiCtx cx{&tmO1, staging};
+        e1.run(taddr, tr.m_t, tr.n_t, r, g.p[1].bn, cx, seq);
+      } else {
+        const EpiCtx cx{&tmO0, staging};
+        e0.run(taddr, tr.m_t, tr.n_t, r, g.p[0].bn, cx, seq);
+      }
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
     }
+    if (Epi::kStaging && lane == 0) bulk_wait<0>();  // this warp's TMA writes have landed
   }
 
   __syncwarp();
@@ -393,11 +524,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ----------------------------------------------------------------------------------------
 // host side
 
-template <int BN, bool A_MN, bool B_MN, class Epi>
-cudaError_t run_gemm(const CUtensorMap& ta, const CUtensorMap& tb, int64_t M, int64_t N, int64_t K, const Epi& epi,
-                     int num_sms, cudaStream_t st) {
-  using S = Shape<BN>;
-  auto kern = tc_gemm_kernel<BN, A_MN, B_MN, Epi>;
+Prob make_prob(int64_t M, int64_t N, int64_t K, int bn, bool a_mn, bool b_mn, bool n_fastest) {
+  Prob q;
+  q.num_m = static_cast<int>((M + BM - 1) / BM);
+  q.num_n = static_cast<int>((N + bn - 1) / bn);
+  q.num_k = static_cast<int>((K + BK - 1) / BK);
+  q.tiles = q.num_m * q.num_n;
+  q.a_mn = a_mn;
+  q.b_mn = b_mn;
+  q.n_fastest = n_fastest;
+  q.bn = bn;
+  return q;
+}
+
+// Launches one or two problems.  `sched` (may be null) is the dynamic tile counter and the
+// host's record of its value, advanced by what this launch consumes (tiles + one final
+// fetch per CTA), so the next launch on the stream knows its base without a reset.
+// maps: A0, B0, A1, B1, O0, O1 (the second problem's entries repeat the first's when absent).
+template <class Epi>
+cudaError_t launch_tc(const CUtensorMap* maps, const Prob* probs, int nprob, const Epi& e0, const Epi& e1,
+                      TileSched* sched, int num_sms, cudaStream_t st) {
+  using S = Shape<Epi::kStaging>;
+  static_assert(S::SMEM <= kSmemMax && S::STAGES >= 3, "shared memory budget");
+  auto kern = tc_gemm_kernel<Epi>;
   static std::atomic<uint64_t> configured{0};  // one bit per device: the attribute is per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -408,14 +557,19 @@ cudaError_t run_gemm(const CUtensorMap& ta, const CUtensorMap& tb, int64_t M, in
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit);
   }
-  Geom g;
-  g.num_m = static_cast<int>((M + BM - 1) / BM);
-  g.num_n = static_cast<int>((N + BN - 1) / BN);
-  g.num_k = static_cast<int>((K + BK - 1) / BK);
-  const int tiles = g.num_m * g.num_n;
-  if (tiles == 0) return cudaSuccess;
-  const int grid = tiles < num_sms ? tiles : num_sms;
-  kern<<<grid, kThreads, S::SMEM, st>>>(ta, tb, g, epi);
+  Geom g{};
+  g.nprob = nprob;
+  g.p[0] = probs[0];
+  g.p[1] = nprob > 1 ? probs[1] : probs[0];
+  g.tiles = probs[0].tiles + (nprob > 1 ? probs[1].tiles : 0);
+  if (g.tiles == 0) return cudaSuccess;
+  const int grid = g.tiles < num_sms ? g.tiles : num_sms;
+  if (sched && sched->counter) {
+    g.counter = sched->counter;
+    g.base = sched->value;
+    sched->value += static_cast<unsigned int>(g.tiles + grid);
+  }
+  kern<<<grid, kThreads, S::SMEM, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], g, e0, e1);
   return cudaGetLastError();
 }
 
@@ -426,28 +580,26 @@ bool map_kmajor(CUtensorMap* m, const void* base, int64_t inner_k, int64_t outer
 bool map_mnmajor(CUtensorMap* m, const void* base, int64_t inner_mn, int64_t outer_k, int64_t ld_elems) {
   return encode_tmap_bf16_2d(m, base, inner_mn, outer_k, ld_elems * 2, 64, 64);
 }
-
-template <bool A_MN, bool B_MN, class Epi>
-cudaError_t run_gemm_bn(int bn, const CUtensorMap& ta, const CUtensorMap& tb, int64_t M, int64_t N, int64_t K,
-                        const Epi& epi, int num_sms, cudaStream_t st) {
-  switch (bn) {
-    case 256: return run_gemm<256, A_MN, B_MN>(ta, tb, M, N, K, epi, num_sms, st);
-    case 192: return run_gemm<192, A_MN, B_MN>(ta, tb, M, N, K, epi, num_sms, st);
-    default: return run_gemm<128, A_MN, B_MN>(ta, tb, M, N, K, epi, num_sms, st);
-  }
+// fp32 output of the TMA epilogue: [rows, cols] with row stride ld, 32 x 32 boxes.
+bool map_out_f32(CUtensorMap* m, const float* base, int64_t cols, int64_t rows, int64_t ld) {
+  return encode_tmap_f32_2d(m, base, cols, rows, ld * 4, 32, 32);
 }
 
-// Tile width over the d columns of dW / dH: the widest of 256 / 192 / 128 that wastes
-// the least of the last tile.
-int pick_bn(int64_t N) {
-  int best = 256;
-  double best_eff = 0.0;
-  for (int bn : {256, 192, 128}) {
-    const int64_t tiles = (N + bn - 1) / bn;
-    const double eff = static_cast<double>(N) / static_cast<double>(tiles * bn);
-    if (eff > best_eff + 0.02) {
-      best_eff = eff;
-      best = bn;
+// Tile width over N: the candidate with the least padded work, counting a fixed cost of 32
+// columns per tile for its ramp-up and epilogue.  An MN-major B needs a multiple of 64;
+// otherwise multiples of 32 are allowed (the epilogues work in 32-column chunks).
+int pick_bn(int64_t N, bool b_mn) {
+  static const int mn[] = {256, 192, 128, 64};
+  static const int km[] = {256, 224, 192, 160, 128, 96, 64, 32};
+  const int* c = b_mn ? mn : km;
+  const int n = b_mn ? 4 : 8;
+  int best = c[0];
+  int64_t best_cost = INT64_MAX;
+  for (int i = 0; i < n; ++i) {
+    const int64_t cost = (N + c[i] - 1) / c[i] * (c[i] + 32);
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = c[i];
     }
   }
   return best;
@@ -457,54 +609,68 @@ int pick_bn(int64_t N) {
 
 cudaError_t tc_fwd_tiles(const void* Hc, const void* W, int64_t rows, int64_t d, int64_t V, float tau,
                          const int32_t* sidx, int32_t K, float* zk, float2* part, int nvt, Ctrl* ctrl,
-                         int num_sms, cudaStream_t st) {
-  CUtensorMap ta, tb;
-  if (!map_kmajor(&ta, Hc, d, rows, d, BM) || !map_kmajor(&tb, W, d, V, d, 256)) return cudaErrorInvalidValue;
+                         TileSched* sched, int num_sms, cudaStream_t st) {
+  CUtensorMap maps[6];
+  if (!map_kmajor(&maps[0], Hc, d, rows, d, BM) || !map_kmajor(&maps[1], W, d, V, d, kTileV))
+    return cudaErrorInvalidValue;
+  maps[2] = maps[4] = maps[0];
+  maps[3] = maps[5] = maps[1];
   FwdEpi e{rows, V, kLog2e / tau, sidx, K, zk, part, nvt, ctrl};
-  return run_gemm<256, false, false>(ta, tb, rows, V, d, e, num_sms, st);
+  const Prob p = make_prob(rows, V, d, kTileV, false, false, false);
+  return launch_tc(maps, &p, 1, e, e, sched, num_sms, st);
 }
 
 cudaError_t tc_bwd_tiles(const void* Hc, const void* W, int64_t rows, int64_t d, int64_t V, int64_t s0, int64_t S,
                          float tau, const int32_t* sidx, const float* sp, int32_t K, const float* lse,
-                         const uint8_t* valid, Ctrl* ctrl, void* G, int64_t ldG, int num_sms,
+                         const uint8_t* valid, Ctrl* ctrl, void* G, int64_t ldG, TileSched* sched, int num_sms,
                          cudaStream_t st) {
   const int64_t s_eff = (V - s0 < S) ? V - s0 : S;
-  CUtensorMap ta, tb;
+  CUtensorMap maps[6];
   const void* Ws = static_cast<const __nv_bfloat16*>(W) + s0 * d;
-  if (!map_kmajor(&ta, Hc, d, rows, d, BM) || !map_kmajor(&tb, Ws, d, s_eff, d, 256)) return cudaErrorInvalidValue;
+  if (!map_kmajor(&maps[0], Hc, d, rows, d, BM) || !map_kmajor(&maps[1], Ws, d, s_eff, d, kTileV))
+    return cudaErrorInvalidValue;
+  maps[2] = maps[4] = maps[0];
+  maps[3] = maps[5] = maps[1];
   BwdEpi e{rows, V, s0, S, ldG, kLog2e / tau, sidx, sp, K, lse, valid, ctrl, static_cast<__nv_bfloat16*>(G)};
-  return run_gemm<256, false, false>(ta, tb, rows, s_eff, d, e, num_sms, st);
+  const Prob p = make_prob(rows, s_eff, d, kTileV, false, false, false);
+  return launch_tc(maps, &p, 1, e, e, sched, num_sms, st);
 }
 
-cudaError_t tc_dW(const void* G, int64_t ldG, const void* Hc, int64_t rows, int64_t d, int64_t S, float* dW_stripe,
-                  int accumulate, Ctrl* ctrl, int num_sms, cudaStream_t st) {
-  // D[S, d] = G^T . Hc: A = G^T stored [rows, S] (MN-major), B = Hc stored [rows, d] (MN-major)
-  CUtensorMap ta, tb;
-  if (!map_mnmajor(&ta, G, S, rows, ldG) || !map_mnmajor(&tb, Hc, d, rows, d)) return cudaErrorInvalidValue;
-  F32Epi e{dW_stripe, d, S, d, accumulate, nullptr, ctrl};
-  return run_gemm_bn<true, true>(pick_bn(d), ta, tb, S, d, rows, e, num_sms, st);
-}
-
-cudaError_t tc_dH(const void* G, int64_t ldG, const void* W_stripe, int64_t rows, int64_t d, int64_t S, float* acc,
-                  int accumulate, void* out_bf16, Ctrl* ctrl, int num_sms, cudaStream_t st) {
-  // D[rows, d] = G . W_s: A = G stored [rows, S] (K-major), B = W_s stored [S, d] (MN-major)
-  CUtensorMap ta, tb;
-  if (!map_kmajor(&ta, G, S, rows, ldG, BM) || !map_mnmajor(&tb, W_stripe, d, S, d)) return cudaErrorInvalidValue;
-  F32Epi e{acc, d, rows, d, accumulate, static_cast<__nv_bfloat16*>(out_bf16), ctrl};
-  return run_gemm_bn<false, true>(pick_bn(d), ta, tb, rows, d, S, e, num_sms, st);
+cudaError_t tc_dW_dH(const void* G, int64_t ldG, const void* HcT, int64_t ldT, const void* W_stripe, int64_t rows,
+                     int64_t d, int64_t S, float* dW_stripe, int dW_accumulate, float* dH_acc, int dH_accumulate,
+                     Ctrl* ctrl, TileSched* sched, int num_sms, cudaStream_t st) {
+  // problem 0, dH^T[d, rows] (+)= W_s^T . G^T: A = W_s stored [S, d] (MN-major), B = G stored
+  //            [rows, S] (K-major); the epilogue writes it transposed into dH_acc[rows, d].
+  // problem 1, dW[S, d] (+)= G^T . Hc: A = G^T stored [rows, S] (MN-major), B = Hc^T stored
+  //            [d, ldT] (K-major).
+  // The dH tiles (K = S) are the longer ones and go first.  N fastest: the CTAs in flight
+  // share their A block.
+  const int bn_h = pick_bn(rows, false), bn_w = pick_bn(d, false);
+  CUtensorMap maps[6];
+  if (!map_mnmajor(&maps[0], W_stripe, d, S, d) || !map_kmajor(&maps[1], G, S, rows, ldG, bn_h) ||
+      !map_mnmajor(&maps[2], G, S, rows, ldG) || !map_kmajor(&maps[3], HcT, rows, d, ldT, bn_w) ||
+      !map_out_f32(&maps[4], dH_acc, d, rows, d) || !map_out_f32(&maps[5], dW_stripe, d, S, d))
+    return cudaErrorInvalidValue;
+  const Prob p[2] = {make_prob(d, rows, S, bn_h, true, false, true), make_prob(S, d, rows, bn_w, true, false, true)};
+  F32Epi eh{d, rows, dH_accumulate, 1, ctrl};
+  F32Epi ew{S, d, dW_accumulate, 0, ctrl};
+  return launch_tc(maps, p, 2, eh, ew, sched, num_sms, st);
 }
 
 cudaError_t tc_debug_gemm(const void* A, const void* B, float* D, int64_t M, int64_t N, int64_t K, int a_mn, int b_mn,
                           int num_sms, cudaStream_t st) {
-  CUtensorMap ta, tb;
-  bool ok = a_mn ? map_mnmajor(&ta, A, M, K, M) : map_kmajor(&ta, A, K, M, K, BM);
-  ok = ok && (b_mn ? map_mnmajor(&tb, B, N, K, N) : map_kmajor(&tb, B, K, N, K, 256));
+  const int bn = pick_bn(N, b_mn != 0);
+  CUtensorMap maps[6];
+  bool ok = a_mn ? map_mnmajor(&maps[0], A, M, K, M) : map_kmajor(&maps[0], A, K, M, K, BM);
+  ok = ok && (b_mn ? map_mnmajor(&maps[1], B, N, K, N) : map_kmajor(&maps[1], B, K, N, K, bn));
+  ok = ok && map_out_f32(&maps[4], D, N, M, N);
   if (!ok) return cudaErrorInvalidValue;
-  F32Epi e{D, N, M, N, 0, nullptr, nullptr};
-  if (!a_mn && !b_mn) return run_gemm<256, false, false>(ta, tb, M, N, K, e, num_sms, st);
-  if (!a_mn && b_mn) return run_gemm_bn<false, true>(pick_bn(N), ta, tb, M, N, K, e, num_sms, st);
-  if (a_mn && !b_mn) return run_gemm<256, true, false>(ta, tb, M, N, K, e, num_sms, st);
-  return run_gemm_bn<true, true>(pick_bn(N), ta, tb, M, N, K, e, num_sms, st);
+  maps[2] = maps[0];
+  maps[3] = maps[1];
+  maps[5] = maps[4];
+  F32Epi e{M, N, 0, 0, nullptr};
+  const Prob p = make_prob(M, N, K, bn, a_mn, b_mn, true);
+  return launch_tc(maps, &p, 1, e, e, nullptr, num_sms, st);
 }
 
 }  // namespace fckl

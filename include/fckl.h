@@ -128,8 +128,7 @@ typedef enum {
   FCKL_K_COMBINE,      /* per-row lse and loss_t from the tile partials */
   FCKL_K_REDUCE,       /* fixed-order mean over rows; N and the gradient scale */
   FCKL_K_BWD_TILES,    /* recomputed logit tiles -> gradient tile G (backward) */
-  FCKL_K_DW,           /* dW[stripe] (+)= G^T . H_chunk */
-  FCKL_K_DH,           /* dH_chunk (+)= G . W[stripe] */
+  FCKL_K_GRAD_GEMM,    /* dW[stripe] (+)= G^T . H_chunk and dH_chunk (+)= G . W[stripe] */
   FCKL_K_OTHER,        /* memsets and casts */
   FCKL_K_NUM_CLASSES
 } fckl_kernel_class;
