@@ -412,15 +412,16 @@ fckl_status fckl_profile_read(int32_t kernel_class, int64_t* launches, double* t
 }
 
 fckl_status fckl_debug_gemm_bf16(const void* A, const void* B, float* D, int64_t M, int64_t N, int64_t K, int32_t a_mn,
-                                 int32_t b_mn, void* stream) {
+                                 int32_t b_mn, int32_t cta_pair, void* stream) {
   if (!A || !B || !D || M < 1 || N < 1 || K < 1) return FCKL_ERR_INVALID_ARG;
+  if (cta_pair && b_mn) return FCKL_ERR_UNSUPPORTED;
   if (M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) || K >= (int64_t(1) << 31)) return FCKL_ERR_INVALID_ARG;
   if ((a_mn ? M : K) % 8 || (b_mn ? N : K) % 8 || N % 8) return FCKL_ERR_UNSUPPORTED;
   if (!aligned(A, 16) || !aligned(B, 16) || !aligned(D, 16)) return FCKL_ERR_UNSUPPORTED;
   int num_sms = 0;
   FCKL_TRY(device_info(&num_sms));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  return step(FCKL_K_OTHER, st, [&] { return tc_debug_gemm(A, B, D, M, N, K, a_mn, b_mn, num_sms, st); });
+  return step(FCKL_K_OTHER, st, [&] { return tc_debug_gemm(A, B, D, M, N, K, a_mn, b_mn, cta_pair, num_sms, st); });
 }
 
 }  // extern "C"

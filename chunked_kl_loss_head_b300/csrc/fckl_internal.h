@@ -96,7 +96,7 @@ cudaError_t tc_dW_dH(const void* G, int64_t ldG, const void* HcT, int64_t ldT, c
                      float* dH_acc, int dH_accumulate, Ctrl* ctrl, TileSched* sched, int num_sms,
                      cudaStream_t st);
 cudaError_t tc_debug_gemm(const void* A, const void* B, float* D, int64_t M, int64_t N, int64_t K,
-                          int a_mn, int b_mn, int num_sms, cudaStream_t st);
+                          int a_mn, int b_mn, int cta_pair, int num_sms, cudaStream_t st);
 
 // ---- host helpers (fckl_api.cu) ----------------------------------------------------------
 bool encode_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,

@@ -1,12 +1,15 @@
 // fckl_tc.cu -- the bf16 path on 5th-generation tensor cores (tcgen05) for sm_103a.
 //
-// One persistent, warp-specialized GEMM engine serves every contraction of the loss:
+// One persistent, warp-specialized GEMM engine serves every contraction of the loss.
+// The loss runs it on CTA pairs (cta_group::2, 256-row tiles split over the two SMs of a
+// TPC); a single-CTA form (128-row tiles) serves the test hook's other operand layouts.
 //   warp 0      TMA producer: hands out tiles and streams 64-deep K slabs of A and B
 //               into a ring of shared-memory stages (128-byte swizzle), completion
 //               tracked by mbarriers;
-//   warp 1      MMA issuer: one thread issues tcgen05.mma (M=128, N=bn, K=16 per
-//               instruction) into one of two TMEM accumulators and commits each stage
-//               back to the producer when the tensor core has read it;
+//   warp 1      MMA issuer: one thread (of the pair's leader CTA) issues tcgen05.mma
+//               (M=128 or 256, N=bn, K=16 per instruction) into one of two TMEM
+//               accumulators and commits each stage back to the producers when the
+//               tensor core has read it;
 //   warps 2-5   epilogue: tcgen05.ld of the finished accumulator, one tile row per
 //               thread, while the MMA warp already fills the other accumulator.
 // The epilogue is what makes each GEMM a step of the loss:
@@ -37,10 +40,12 @@ constexpr int kTmemCols = 512;    // two accumulators of up to 256 fp32 columns
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kSmemMax = 232448;  // opt-in dynamic shared memory per block
 
-template <int STAGING>
+// Shared-memory plan of one CTA.  CG = CTAs per tile (1, or 2 for a CTA pair, where each
+// CTA holds 128 rows of A and half of the tile's B rows).
+template <int STAGING, int CG>
 struct Shape {
   static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = kBNMax * BK * 2;
+  static constexpr int B_BYTES = (kBNMax / CG) * BK * 2;
   static constexpr int STAGE = A_BYTES + B_BYTES;
   static constexpr int BAR_BYTES = 512;
   static constexpr int FIT = (kSmemMax - 1024 - BAR_BYTES - STAGING) / STAGE;
@@ -98,17 +103,30 @@ __device__ __forceinline__ TileRef tile_of(const Geom& g, int t) {
   return r;
 }
 
-// Shared flag: a role that gave up on a wait tells the others to stop waiting.
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                              Ctrl* ctrl) {
-  if (mbar_try_wait(bar, parity)) return true;
+// Shared flag: a role that gave up on a wait tells the others to stop waiting (in a CTA
+// pair, the peer's flag is raised too).  CLUSTER selects an acquire at cluster scope, for
+// phases that the peer CTA completes.
+struct AbortFlag {
+  volatile int* local;
+  uint32_t peer;  // shared::cluster address of the peer's flag, 0 without a peer
+
+  __device__ __forceinline__ void raise() const {
+    *local = 1;
+    if (peer) st_shared_cluster_u32(peer, 1u);
+  }
+};
+
+template <bool CLUSTER = false>
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, const AbortFlag& af, Ctrl* ctrl) {
+  auto try_wait = [&] { return CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
+  if (try_wait()) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t i = 0;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (try_wait()) return true;
     if ((i & 63) == 63) {
-      if (*abort_flag) return false;
+      if (*af.local) return false;
       if (global_ns() - t0 > FCKL_WAIT_NS) {
-        *abort_flag = 1;
+        af.raise();
         if (ctrl) set_status(ctrl, FCKL_ERR_TIMEOUT);
         return false;
       }
@@ -319,24 +337,36 @@ struct F32Epi {
 // The engine.  Per problem, a_mn / b_mn select the operand layouts:
 //   A K-major: A[m, k] at row m of a [M, K] tensor (TMA box 64 x 128);
 //   A MN-major: A[m, k] at row k of a [K, M] tensor (two 64 x 64 boxes per stage);
-//   B K-major: B[n, k] at row n of a [N, K] tensor (box 64 x bn), so D = A . B^T;
-//   B MN-major: B[k, n] at row k of a [K, N] tensor (bn/64 boxes of 64 x 64).
+//   B K-major: B[n, k] at row n of a [N, K] tensor (box 64 x bn/CG), so D = A . B^T;
+//   B MN-major: B[k, n] at row k of a [K, N] tensor (bn/64 boxes of 64 x 64; CG = 1 only).
 // (On this part an MN-major B operand costs 12-25% of MMA throughput and an MN-major A
 // nothing, so the loss arranges its contractions to have K-major B operands.)
-// Tiles are handed out by the producer warp: from the global counter when there is one
-// (each CTA takes the next tile when it is ready for one, which balances tiles of
-// different cost), else round-robin; the tile sequence reaches the MMA warp and the
-// epilogue warps through a small shared-memory queue.
+//
+// CG = 2 runs each tile on a CTA pair (a cluster of two CTAs on the two SMs of a TPC):
+// the tile is 256 rows x bn, each CTA loads its 128 rows of A and half of the bn rows of
+// B, and the leader (rank 0) issues cta_group::2 MMAs that read both CTAs' shared memory
+// and write each CTA's 128 accumulator rows into its own TMEM.  Per SM, a 64-deep k-block
+// then costs 32 KB of operand traffic instead of 48 KB for the same 128 x 256 x 64 MMA
+// work, which is what the L2 -> SM path can sustain.  Both CTAs' loads signal the leader's
+// `full` barrier; the leader's commits arrive on both CTAs' `empty` and `tfull` barriers;
+// the peer's epilogue warps release accumulators on the leader's `tempty` barrier.
+//
+// Tiles are handed out by the (leader's) producer warp: from the global counter when
+// there is one (each CTA or pair takes the next tile when it is ready for one, which
+// balances tiles of different cost), else round-robin; the tile sequence reaches the MMA
+// warp and the epilogue warps of both CTAs through a small shared-memory queue.
 constexpr int kQueue = 4;
+constexpr int kEpiWarps = kEpiThreads / 32;
 
-template <class Epi>
+template <class Epi, int CG>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmB0,
                    const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
                    const __grid_constant__ CUtensorMap tmO0, const __grid_constant__ CUtensorMap tmO1, Geom g,
                    Epi e0, Epi e1) {
-  using S = Shape<Epi::kStaging>;
-  constexpr uint32_t IDESC = idesc_bf16_f32(BM, 8, false, false) & ~(0x3Fu << 17);  // N filled per problem
+  static_assert(CG == 1 || CG == 2, "one CTA or a CTA pair per tile");
+  using S = Shape<Epi::kStaging, CG>;
+  constexpr uint32_t IDESC = idesc_bf16_f32(BM * CG, 8, false, false) & ~(0x3Fu << 17);  // N set per problem
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -350,9 +380,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* qempty = qfull + kQueue;
   int* tileq = reinterpret_cast<int*>(qempty + kQueue);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tileq + kQueue);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* abort_local = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+  const int unit = CG == 2 ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int units = CG == 2 ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  // shared::cluster addresses in the other CTA of the pair (unused when CG == 1)
+  auto remote = [&](const void* p, uint32_t r) { return mapa_shared(smem_u32(p), r); };
+  const AbortFlag af{abort_local, CG == 2 ? remote(const_cast<int*>(abort_local), rank ^ 1u) : 0u};
+
   Ctrl* ctrl = e0.ctrl;
   if (threadIdx.x == 0) {
     for (int s = 0; s < S::STAGES; ++s) {
@@ -361,13 +399,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], kEpiThreads);
+      mbar_init(&tempty[a], CG * kEpiWarps);
     }
+    // consumers of a queue slot, one arrival per warp: the leader's MMA warp and the
+    // epilogue warps of every CTA, plus the peer's producer
     for (int q = 0; q < kQueue; ++q) {
       mbar_init(&qfull[q], 1);
-      mbar_init(&qempty[q], 1 + kEpiThreads);
+      mbar_init(&qempty[q], 1 + CG * kEpiWarps + (CG - 1));
     }
-    *abort_flag = 0;
+    *abort_local = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
   }
@@ -382,69 +422,106 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, kTmemCols);
-    tmem_relinquish();
+    if (CG == 2) {
+      tmem_alloc_pair(tmem_slot, kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if (CG == 2) cluster_sync(); else __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
     if (lane == 0) {
       uint32_t it = 0;
-      int next_static = blockIdx.x;
+      int next_static = unit;
+      const uint32_t full_leader0 = CG == 2 ? remote(&full[0], 0) : 0u;
       for (int i = 0;; ++i) {
         const int slot = i % kQueue;
-        if (!wait_or_abort(&qempty[slot], ((i / kQueue) & 1) ^ 1, abort_flag, ctrl)) break;
+        const uint32_t qph = (i / kQueue) & 1;
         int t;
-        if (g.counter) {
-          t = static_cast<int>(atomicAdd(g.counter, 1u) - g.base);
+        if (leader) {
+          if (!wait_or_abort(&qempty[slot], qph ^ 1, af, ctrl)) break;
+          if (g.counter) {
+            t = static_cast<int>(atomicAdd(g.counter, 1u) - g.base);
+          } else {
+            t = next_static;
+            next_static += units;
+          }
+          if (t >= g.tiles) t = -1;
+          tileq[slot] = t;
+          mbar_arrive(&qfull[slot]);
+          if (CG == 2) {
+            st_shared_cluster_u32(remote(&tileq[slot], 1), static_cast<uint32_t>(t));
+            mbar_arrive_cluster(remote(&qfull[slot], 1));
+          }
         } else {
-          t = next_static;
-          next_static += gridDim.x;
+          if (!wait_or_abort<true>(&qfull[slot], qph, af, ctrl)) break;
+          t = tileq[slot];
+          mbar_arrive_cluster(remote(&qempty[slot], 0));
         }
-        if (t >= g.tiles) t = -1;
-        tileq[slot] = t;
-        mbar_arrive(&qfull[slot]);
         if (t < 0) break;
         const TileRef tr = tile_of(g, t);
         const Prob q = tr.prob ? g.p[1] : g.p[0];
         const CUtensorMap* ta = tr.prob ? &tmA1 : &tmA0;
         const CUtensorMap* tb = tr.prob ? &tmB1 : &tmB0;
-        const uint32_t tx = S::A_BYTES + static_cast<uint32_t>(q.bn) * BK * 2;
+        const uint32_t tx = static_cast<uint32_t>(CG * S::A_BYTES + q.bn * BK * 2);  // both CTAs' boxes
+        const int m_row = (tr.m_t * CG + static_cast<int>(rank)) * BM;
+        const int b_rows = q.bn / CG;
         bool ok = true;
         for (int kb = 0; kb < q.num_k; ++kb, ++it) {
           const int s = it % S::STAGES;
           const uint32_t ph = (it / S::STAGES) & 1;
-          if (!wait_or_abort(&empty[s], ph ^ 1, abort_flag, ctrl)) {
+          if (!wait_or_abort(&empty[s], ph ^ 1, af, ctrl)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[s], tx);
+          if (leader) mbar_arrive_expect_tx(&full[s], tx);
           uint8_t* a = sA + s * S::A_BYTES;
           uint8_t* b = sB + s * S::B_BYTES;
-          if (!q.a_mn) {
-            tma_load_2d(a, ta, &full[s], kb * BK, tr.m_t * BM);
+          if (CG == 2) {
+            const uint32_t fb = full_leader0 + static_cast<uint32_t>(s) * 8u;
+            if (!q.a_mn) {
+              tma_load_2d_pair(a, ta, fb, kb * BK, m_row);
+            } else {
+              tma_load_2d_pair(a, ta, fb, m_row, kb * BK);
+              tma_load_2d_pair(a + 8192, ta, fb, m_row + 64, kb * BK);
+            }
+            tma_load_2d_pair(b, tb, fb, kb * BK, tr.n_t * q.bn + static_cast<int>(rank) * b_rows);
           } else {
-            tma_load_2d(a, ta, &full[s], tr.m_t * BM, kb * BK);
-            tma_load_2d(a + 8192, ta, &full[s], tr.m_t * BM + 64, kb * BK);
-          }
-          if (!q.b_mn) {
-            tma_load_2d(b, tb, &full[s], kb * BK, tr.n_t * q.bn);
-          } else {
-            for (int h = 0; h < q.bn / 64; ++h) tma_load_2d(b + h * 8192, tb, &full[s], tr.n_t * q.bn + h * 64, kb * BK);
+            if (!q.a_mn) {
+              tma_load_2d(a, ta, &full[s], kb * BK, m_row);
+            } else {
+              tma_load_2d(a, ta, &full[s], m_row, kb * BK);
+              tma_load_2d(a + 8192, ta, &full[s], m_row + 64, kb * BK);
+            }
+            if (!q.b_mn) {
+              tma_load_2d(b, tb, &full[s], kb * BK, tr.n_t * q.bn);
+            } else {
+              for (int h = 0; h < q.bn / 64; ++h)
+                tma_load_2d(b + h * 8192, tb, &full[s], tr.n_t * q.bn + h * 64, kb * BK);
+            }
           }
         }
         if (!ok) break;
       }
+      // Drain: every stage's last fill has been consumed (the commits that say so have
+      // landed on this CTA's barriers) before the CTA may leave.
+      for (uint32_t j = 0; j < S::STAGES && j < it; ++j) {
+        const uint32_t f = it - 1 - j;
+        if (!wait_or_abort(&empty[f % S::STAGES], (f / S::STAGES) & 1, af, ctrl)) break;
+      }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       uint32_t it = 0;
       for (int i = 0;; ++i) {
         const int slot = i % kQueue;
-        if (!wait_or_abort(&qfull[slot], (i / kQueue) & 1, abort_flag, ctrl)) break;
+        if (!wait_or_abort(&qfull[slot], (i / kQueue) & 1, af, ctrl)) break;
         const int t = tileq[slot];
         mbar_arrive(&qempty[slot]);
         if (t < 0) break;
@@ -453,14 +530,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t idesc = IDESC | (static_cast<uint32_t>(q.bn >> 3) << 17) |
                                (static_cast<uint32_t>(q.a_mn) << 15) | (static_cast<uint32_t>(q.b_mn) << 16);
         const uint32_t acc = i & 1, use = i >> 1;
-        if (!wait_or_abort(&tempty[acc], (use & 1) ^ 1, abort_flag, ctrl)) break;
+        if (!wait_or_abort(&tempty[acc], (use & 1) ^ 1, af, ctrl)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * kBNMax;
         bool ok = true;
         for (int kb = 0; kb < q.num_k; ++kb, ++it) {
           const int s = it % S::STAGES;
           const uint32_t ph = (it / S::STAGES) & 1;
-          if (!wait_or_abort(&full[s], ph, abort_flag, ctrl)) {
+          if (!wait_or_abort(&full[s], ph, af, ctrl)) {
             ok = false;
             break;
           }
@@ -473,60 +550,87 @@ __global__ void __launch_bounds__(kThreads, 1)
                 q.a_mn ? sdesc_sw128(a_base + k * 2048, 8192, 1024) : sdesc_sw128(a_base + k * 32, 16, 1024);
             const uint64_t bd =
                 q.b_mn ? sdesc_sw128(b_base + k * 2048, 8192, 1024) : sdesc_sw128(b_base + k * 32, 16, 1024);
-            umma_f16(d_tmem, ad, bd, idesc, (kb | k) != 0);
+            if (CG == 2) umma_f16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0);
+            else umma_f16(d_tmem, ad, bd, idesc, (kb | k) != 0);
           }
-          umma_commit(&empty[s]);
+          if (CG == 2) umma_commit_pair(&empty[s], 0x3);
+          else umma_commit(&empty[s]);
         }
         if (!ok) break;
-        umma_commit(&tfull[acc]);
+        if (CG == 2) umma_commit_pair(&tfull[acc], 0x3);
+        else umma_commit(&tfull[acc]);
       }
     }
   } else {
     const int quad = warp & 3;  // TMEM lane quadrant this warp may access
     const int r = quad * 32 + lane;
     uint32_t seq = 0;  // staging-buffer sequence of this warp (TMA epilogues)
+    const uint32_t m_off = rank;
+    // Lane 0 of each warp waits and reads the queue; the warp follows it (tcgen05.ld is
+    // warp-collective, so the lanes must not part ways on a timeout).
     for (int i = 0;; ++i) {
       const int slot = i % kQueue;
-      if (!wait_or_abort(&qfull[slot], (i / kQueue) & 1, abort_flag, ctrl)) break;
-      const int t = tileq[slot];
-      mbar_arrive(&qempty[slot]);
-      if (t < 0) break;
+      int t = -1;
+      int ok = 1;
+      if (lane == 0) {
+        ok = wait_or_abort<CG == 2>(&qfull[slot], (i / kQueue) & 1, af, ctrl);
+        if (ok) {
+          t = tileq[slot];
+          if (leader) mbar_arrive(&qempty[slot]);
+          else mbar_arrive_cluster(remote(&qempty[slot], 0));
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      t = __shfl_sync(0xffffffffu, t, 0);
+      if (!ok || t < 0) break;
       const TileRef tr = tile_of(g, t);
       const uint32_t acc = i & 1, use = i >> 1;
-      if (!wait_or_abort(&tfull[acc], use & 1, abort_flag, ctrl)) break;
+      if (lane == 0) ok = wait_or_abort(&tfull[acc], use & 1, af, ctrl);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      __syncwarp();
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * kBNMax;
+      const int m_blk = tr.m_t * CG + static_cast<int>(m_off);  // this CTA's 128-row block
       if (tr.prob) {
         const EpiCtx cx{&tmO1, staging};
-        e1.run(taddr, tr.m_t, tr.n_t, r, g.p[1].bn, cx, seq);
+        e1.run(taddr, m_blk, tr.n_t, r, g.p[1].bn, cx, seq);
       } else {
         const EpiCtx cx{&tmO0, staging};
-        e0.run(taddr, tr.m_t, tr.n_t, r, g.p[0].bn, cx, seq);
+        e0.run(taddr, m_blk, tr.n_t, r, g.p[0].bn, cx, seq);
       }
       tc_fence_before();
-      mbar_arrive(&tempty[acc]);
+      __syncwarp();
+      if (lane == 0) {
+        if (leader) mbar_arrive(&tempty[acc]);
+        else mbar_arrive_cluster(remote(&tempty[acc], 0));
+      }
     }
     if (Epi::kStaging && lane == 0) bulk_wait<0>();  // this warp's TMA writes have landed
   }
 
   __syncwarp();
   tc_fence_before();
-  __syncthreads();
+  if (CG == 2) cluster_sync(); else __syncthreads();
   tc_fence_after();
-  if (*abort_flag) {
+  if (*abort_local) {
     // let copies and MMAs already in flight land before the memory they target goes away
     const uint64_t t0 = global_ns();
     while (global_ns() - t0 < 2000000ull) __nanosleep(1000);
   }
-  if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+  if (warp == 1) {
+    if (CG == 2) tmem_dealloc_pair(tmem_base, kTmemCols);
+    else tmem_dealloc(tmem_base, kTmemCols);
+  }
 }
 
 // ----------------------------------------------------------------------------------------
 // host side
 
-Prob make_prob(int64_t M, int64_t N, int64_t K, int bn, bool a_mn, bool b_mn, bool n_fastest) {
+// M granularity of a tile: 128 rows for one CTA, 256 for a pair.
+Prob make_prob(int64_t M, int64_t N, int64_t K, int bn, bool a_mn, bool b_mn, bool n_fastest, int cg) {
   Prob q;
-  q.num_m = static_cast<int>((M + BM - 1) / BM);
+  q.num_m = static_cast<int>((M + BM * cg - 1) / (BM * cg));
   q.num_n = static_cast<int>((N + bn - 1) / bn);
   q.num_k = static_cast<int>((K + BK - 1) / BK);
   q.tiles = q.num_m * q.num_n;
@@ -537,40 +641,92 @@ Prob make_prob(int64_t M, int64_t N, int64_t K, int bn, bool a_mn, bool b_mn, bo
   return q;
 }
 
+// Per-device launch facts of one kernel instantiation: the shared-memory attribute is set
+// once per device and the number of co-resident units (CTAs, or clusters of two) queried.
+struct KernelInfo {
+  std::atomic<uint64_t> configured{0};
+  int units[64] = {};
+};
+
+template <class Epi, int CG>
+cudaError_t kernel_units(int dev, int num_sms, int* units) {
+  using S = Shape<Epi::kStaging, CG>;
+  static KernelInfo info;
+  auto kern = tc_gemm_kernel<Epi, CG>;
+  const uint64_t bit = uint64_t(1) << (dev & 63);
+  if (!(info.configured.load() & bit)) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
+    if (e != cudaSuccess) return e;
+    int n = num_sms;
+    if (CG == 2) {
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.gridDim = dim3(static_cast<unsigned>(num_sms / 2 * 2));
+      cfg.blockDim = dim3(kThreads);
+      cfg.dynamicSmemBytes = S::SMEM;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      e = cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(kern), &cfg);
+      if (e != cudaSuccess) return e;
+    }
+    info.units[dev & 63] = n;
+    info.configured.fetch_or(bit);
+  }
+  *units = info.units[dev & 63];
+  return cudaSuccess;
+}
+
 // Launches one or two problems.  `sched` (may be null) is the dynamic tile counter and the
 // host's record of its value, advanced by what this launch consumes (tiles + one final
-// fetch per CTA), so the next launch on the stream knows its base without a reset.
-// maps: A0, B0, A1, B1, O0, O1 (the second problem's entries repeat the first's when absent).
-template <class Epi>
+// fetch per scheduling unit), so the next launch on the stream knows its base without a
+// reset.  maps: A0, B0, A1, B1, O0, O1 (the second problem's entries repeat the first's
+// when absent).  The problems must have been made with the same `CG`.
+template <int CG, class Epi>
 cudaError_t launch_tc(const CUtensorMap* maps, const Prob* probs, int nprob, const Epi& e0, const Epi& e1,
                       TileSched* sched, int num_sms, cudaStream_t st) {
-  using S = Shape<Epi::kStaging>;
+  using S = Shape<Epi::kStaging, CG>;
   static_assert(S::SMEM <= kSmemMax && S::STAGES >= 3, "shared memory budget");
-  auto kern = tc_gemm_kernel<Epi>;
-  static std::atomic<uint64_t> configured{0};  // one bit per device: the attribute is per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  const uint64_t bit = uint64_t(1) << (dev & 63);
-  if (!(configured.load() & bit)) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
-    if (e != cudaSuccess) return e;
-    configured.fetch_or(bit);
-  }
+  int max_units = 0;
+  e = kernel_units<Epi, CG>(dev, num_sms, &max_units);
+  if (e != cudaSuccess) return e;
+  if (max_units < 1) return cudaErrorInvalidConfiguration;
   Geom g{};
   g.nprob = nprob;
   g.p[0] = probs[0];
   g.p[1] = nprob > 1 ? probs[1] : probs[0];
   g.tiles = probs[0].tiles + (nprob > 1 ? probs[1].tiles : 0);
   if (g.tiles == 0) return cudaSuccess;
-  const int grid = g.tiles < num_sms ? g.tiles : num_sms;
+  const int units = g.tiles < max_units ? g.tiles : max_units;
   if (sched && sched->counter) {
     g.counter = sched->counter;
     g.base = sched->value;
-    sched->value += static_cast<unsigned int>(g.tiles + grid);
+    sched->value += static_cast<unsigned int>(g.tiles + units);
   }
-  kern<<<grid, kThreads, S::SMEM, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], g, e0, e1);
-  return cudaGetLastError();
+  auto kern = tc_gemm_kernel<Epi, CG>;
+  if (CG == 1) {
+    kern<<<units, kThreads, S::SMEM, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], g, e0, e1);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * units));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = S::SMEM;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], g, e0, e1);
 }
 
 // Operand tensor maps.  K-major: rows of the operand are `outer`, K is `inner`.
@@ -587,7 +743,8 @@ bool map_out_f32(CUtensorMap* m, const float* base, int64_t cols, int64_t rows, 
 
 // Tile width over N: the candidate with the least padded work, counting a fixed cost of 32
 // columns per tile for its ramp-up and epilogue.  An MN-major B needs a multiple of 64;
-// otherwise multiples of 32 are allowed (the epilogues work in 32-column chunks).
+// otherwise multiples of 32 are allowed (the epilogues work in 32-column chunks; a CTA
+// pair's half of B is then a multiple of 16 rows, whole 8-row swizzle atoms).
 int pick_bn(int64_t N, bool b_mn) {
   static const int mn[] = {256, 192, 128, 64};
   static const int km[] = {256, 224, 192, 160, 128, 96, 64, 32};
@@ -605,19 +762,23 @@ int pick_bn(int64_t N, bool b_mn) {
   return best;
 }
 
+// The loss runs every contraction on CTA pairs; the single-CTA engine serves the test hook
+// for operand layouts the pair engine does not take (an MN-major B).
+constexpr int kLossCG = 2;
+
 }  // namespace
 
 cudaError_t tc_fwd_tiles(const void* Hc, const void* W, int64_t rows, int64_t d, int64_t V, float tau,
                          const int32_t* sidx, int32_t K, float* zk, float2* part, int nvt, Ctrl* ctrl,
                          TileSched* sched, int num_sms, cudaStream_t st) {
   CUtensorMap maps[6];
-  if (!map_kmajor(&maps[0], Hc, d, rows, d, BM) || !map_kmajor(&maps[1], W, d, V, d, kTileV))
+  if (!map_kmajor(&maps[0], Hc, d, rows, d, BM) || !map_kmajor(&maps[1], W, d, V, d, kTileV / kLossCG))
     return cudaErrorInvalidValue;
   maps[2] = maps[4] = maps[0];
   maps[3] = maps[5] = maps[1];
   FwdEpi e{rows, V, kLog2e / tau, sidx, K, zk, part, nvt, ctrl};
-  const Prob p = make_prob(rows, V, d, kTileV, false, false, false);
-  return launch_tc(maps, &p, 1, e, e, sched, num_sms, st);
+  const Prob p = make_prob(rows, V, d, kTileV, false, false, false, kLossCG);
+  return launch_tc<kLossCG>(maps, &p, 1, e, e, sched, num_sms, st);
 }
 
 cudaError_t tc_bwd_tiles(const void* Hc, const void* W, int64_t rows, int64_t d, int64_t V, int64_t s0, int64_t S,
@@ -627,13 +788,13 @@ cudaError_t tc_bwd_tiles(const void* Hc, const void* W, int64_t rows, int64_t d,
   const int64_t s_eff = (V - s0 < S) ? V - s0 : S;
   CUtensorMap maps[6];
   const void* Ws = static_cast<const __nv_bfloat16*>(W) + s0 * d;
-  if (!map_kmajor(&maps[0], Hc, d, rows, d, BM) || !map_kmajor(&maps[1], Ws, d, s_eff, d, kTileV))
+  if (!map_kmajor(&maps[0], Hc, d, rows, d, BM) || !map_kmajor(&maps[1], Ws, d, s_eff, d, kTileV / kLossCG))
     return cudaErrorInvalidValue;
   maps[2] = maps[4] = maps[0];
   maps[3] = maps[5] = maps[1];
   BwdEpi e{rows, V, s0, S, ldG, kLog2e / tau, sidx, sp, K, lse, valid, ctrl, static_cast<__nv_bfloat16*>(G)};
-  const Prob p = make_prob(rows, s_eff, d, kTileV, false, false, false);
-  return launch_tc(maps, &p, 1, e, e, sched, num_sms, st);
+  const Prob p = make_prob(rows, s_eff, d, kTileV, false, false, false, kLossCG);
+  return launch_tc<kLossCG>(maps, &p, 1, e, e, sched, num_sms, st);
 }
 
 cudaError_t tc_dW_dH(const void* G, int64_t ldG, const void* HcT, int64_t ldT, const void* W_stripe, int64_t rows,
@@ -643,34 +804,39 @@ cudaError_t tc_dW_dH(const void* G, int64_t ldG, const void* HcT, int64_t ldT, c
   //            [rows, S] (K-major); the epilogue writes it transposed into dH_acc[rows, d].
   // problem 1, dW[S, d] (+)= G^T . Hc: A = G^T stored [rows, S] (MN-major), B = Hc^T stored
   //            [d, ldT] (K-major).
-  // The dH tiles (K = S) are the longer ones and go first.  N fastest: the CTAs in flight
+  // The dH tiles (K = S) are the longer ones and go first.  N fastest: the units in flight
   // share their A block.
+  constexpr int cg = kLossCG;
   const int bn_h = pick_bn(rows, false), bn_w = pick_bn(d, false);
   CUtensorMap maps[6];
-  if (!map_mnmajor(&maps[0], W_stripe, d, S, d) || !map_kmajor(&maps[1], G, S, rows, ldG, bn_h) ||
-      !map_mnmajor(&maps[2], G, S, rows, ldG) || !map_kmajor(&maps[3], HcT, rows, d, ldT, bn_w) ||
+  if (!map_mnmajor(&maps[0], W_stripe, d, S, d) || !map_kmajor(&maps[1], G, S, rows, ldG, bn_h / cg) ||
+      !map_mnmajor(&maps[2], G, S, rows, ldG) || !map_kmajor(&maps[3], HcT, rows, d, ldT, bn_w / cg) ||
       !map_out_f32(&maps[4], dH_acc, d, rows, d) || !map_out_f32(&maps[5], dW_stripe, d, S, d))
     return cudaErrorInvalidValue;
-  const Prob p[2] = {make_prob(d, rows, S, bn_h, true, false, true), make_prob(S, d, rows, bn_w, true, false, true)};
+  const Prob p[2] = {make_prob(d, rows, S, bn_h, true, false, true, cg),
+                     make_prob(S, d, rows, bn_w, true, false, true, cg)};
   F32Epi eh{d, rows, dH_accumulate, 1, ctrl};
   F32Epi ew{S, d, dW_accumulate, 0, ctrl};
-  return launch_tc(maps, p, 2, eh, ew, sched, num_sms, st);
+  return launch_tc<cg>(maps, p, 2, eh, ew, sched, num_sms, st);
 }
 
 cudaError_t tc_debug_gemm(const void* A, const void* B, float* D, int64_t M, int64_t N, int64_t K, int a_mn, int b_mn,
-                          int num_sms, cudaStream_t st) {
+                          int cta_pair, int num_sms, cudaStream_t st) {
+  const int cg = cta_pair ? 2 : 1;
+  if (cg == 2 && b_mn) return cudaErrorInvalidValue;
   const int bn = pick_bn(N, b_mn != 0);
   CUtensorMap maps[6];
   bool ok = a_mn ? map_mnmajor(&maps[0], A, M, K, M) : map_kmajor(&maps[0], A, K, M, K, BM);
-  ok = ok && (b_mn ? map_mnmajor(&maps[1], B, N, K, N) : map_kmajor(&maps[1], B, K, N, K, bn));
+  ok = ok && (b_mn ? map_mnmajor(&maps[1], B, N, K, N) : map_kmajor(&maps[1], B, K, N, K, bn / cg));
   ok = ok && map_out_f32(&maps[4], D, N, M, N);
   if (!ok) return cudaErrorInvalidValue;
   maps[2] = maps[0];
   maps[3] = maps[1];
   maps[5] = maps[4];
   F32Epi e{M, N, 0, 0, nullptr};
-  const Prob p = make_prob(M, N, K, bn, a_mn, b_mn, true);
-  return launch_tc(maps, &p, 1, e, e, nullptr, num_sms, st);
+  const Prob p = make_prob(M, N, K, bn, a_mn, b_mn, true, cg);
+  if (cg == 2) return launch_tc<2>(maps, &p, 1, e, e, nullptr, num_sms, st);
+  return launch_tc<1>(maps, &p, 1, e, e, nullptr, num_sms, st);
 }
 
 }  // namespace fckl

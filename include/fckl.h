@@ -149,9 +149,12 @@ FCKL_API fckl_status fckl_profile_read(int32_t kernel_class, int64_t* launches, 
  * = A . B with bf16 operands on the same tensor-core path the loss uses.
  * a_mn == 0: A is [M, K] (K contiguous); a_mn == 1: A is stored [K, M].
  * b_mn == 0: B is stored [N, K] (so D = A . B^T); b_mn == 1: B is stored [K, N].
+ * cta_pair != 0 runs 256-row tiles on CTA pairs (cta_group::2), the engine the loss uses;
+ * 0 runs 128-row tiles on single CTAs.  The pair engine takes only b_mn == 0
+ * (FCKL_ERR_UNSUPPORTED otherwise).
  * M, N, K >= 1; M or N contiguous extents need multiples of 8 elements. */
 FCKL_API fckl_status fckl_debug_gemm_bf16(const void* A, const void* B, float* D, int64_t M, int64_t N,
-                                 int64_t K, int32_t a_mn, int32_t b_mn, void* stream);
+                                 int64_t K, int32_t a_mn, int32_t b_mn, int32_t cta_pair, void* stream);
 
 /* ---- forward without a workspace --------------------------------------------------------
  * The pages describe no such call: it has no counterpart in the method and exists only for

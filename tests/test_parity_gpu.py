@@ -51,9 +51,9 @@ def check(x, got, grad_loss=1.0, label=""):
 # ------------------------------------------------------------------------------ GEMM engine
 
 
-@pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 0), (1, 1)])
-@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (304, 520, 200), (1000, 2880, 136), (8, 8, 8)])
-def test_engine_gemm_layouts(a_mn, b_mn, M, N, K):
+@pytest.mark.parametrize("a_mn,b_mn,pair", [(0, 0, 1), (1, 0, 1), (0, 0, 0), (0, 1, 0), (1, 0, 0), (1, 1, 0)])
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (304, 520, 200), (1000, 2880, 136), (8, 8, 8), (520, 224, 4104)])
+def test_engine_gemm_layouts(a_mn, b_mn, pair, M, N, K):
     g = torch.Generator().manual_seed(M * 7 + N + K)
     A = torch.randn((K, M) if a_mn else (M, K), generator=g).to(torch.bfloat16)
     B = torch.randn((K, N) if b_mn else (N, K), generator=g).to(torch.bfloat16)
@@ -61,7 +61,7 @@ def test_engine_gemm_layouts(a_mn, b_mn, M, N, K):
     B64 = B.double() if b_mn else B.double().T
     ref = (A64 @ B64).numpy()
     D = torch.full((M, N), float("nan"), device="cuda")
-    api.fckl_debug_gemm_bf16(A.cuda(), B.cuda(), D, M, N, K, a_mn, b_mn)
+    api.fckl_debug_gemm_bf16(A.cuda(), B.cuda(), D, M, N, K, a_mn, b_mn, pair)
     torch.cuda.synchronize()
     err = rel_max(D.cpu().numpy(), ref)
     assert err <= 1e-5, err
