@@ -145,6 +145,57 @@ def run_reference(args, cfg):
     print(json.dumps(line), flush=True)
 
 
+def run_memory_curve(args, cfg):
+    """Peak device memory of one fused fwd+bwd (inputs, outputs and workspace included) as
+    the token count grows, next to the size of the one dense [T x V] bf16 tensor the
+    method never builds (the pages' isolated loss benchmark compares memory this way,
+    axbrief.com, "Quantifying the Efficiency Gain: 15.6x VRAM Reduction")."""
+    import torch
+
+    from chunked_kl_loss_head_b300 import api
+    from chunked_kl_loss_head_b300.memory import dense_logit_bytes
+    from gen import make_inputs
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    chunk = args.chunk or cfg.chunks[0]
+    points = []
+    for T in (int(v) for v in args.memory_curve.split(",")):
+        c = cfg.with_(name=f"{cfg.name}[T={T}]", T=T, seq_len=min(cfg.seq_len or T, T))
+        x = make_inputs(c)
+        tdt = torch.bfloat16 if c.dtype == "bf16" else torch.float32
+
+        def to_dev(a):
+            if a.dtype == np.uint16:
+                return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+            return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+        torch.cuda.synchronize(dev)
+        torch.cuda.empty_cache()
+        torch.cuda.reset_peak_memory_stats(dev)
+        free0, _ = torch.cuda.mem_get_info(dev)
+        g = {k: to_dev(x[k]) for k in ("H", "W", "topk_idx", "topk_logits", "valid")}
+        del x
+        ws = api.workspace(T, c.d, c.V, c.K, chunk, tdt, dev)
+        loss, lse = api.forward(g["H"], g["W"], g["topk_idx"], g["topk_logits"], g["valid"], c.tau, chunk, ws=ws)
+        dH, dW = api.backward(g["H"], g["W"], g["topk_idx"], g["topk_logits"], g["valid"], lse, c.tau, chunk,
+                              ws=ws)
+        torch.cuda.synchronize(dev)
+        status = api.fckl_get_error(ws)
+        if status != 0:
+            raise SystemExit(f"device status: {api.fckl_status_string(status)}")
+        peak = torch.cuda.max_memory_allocated(dev)
+        free1, _ = torch.cuda.mem_get_info(dev)
+        points.append(dict(T=T, peak_device_gib=peak / 2 ** 30,
+                           nontorch_device_gib=max(0.0, (free0 - free1 - peak) / 2 ** 30),
+                           workspace_gib=ws.numel() / 2 ** 30, loss=float(loss.item()),
+                           dense_TxV_bf16_gib=dense_logit_bytes(T, c.V) / 2 ** 30))
+        del g, ws, loss, lse, dH, dW
+    print(json.dumps(dict(metric="peak device GiB of one fused fwd+bwd vs tokens", unit="GiB",
+                          config=dict(workload=cfg.name, d=cfg.d, V=cfg.V, K=cfg.K, chunk=chunk),
+                          points=points)), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -158,6 +209,9 @@ def main():
     ap.add_argument("--shape", default="", help="override T,d,V,K of the workload (e.g. a small ncu case)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--memory-curve", default="",
+                    help="comma-separated token counts: peak device memory of one fwd+bwd of the workload's "
+                         "shape at each T (one JSON line), instead of the timing run")
     args = ap.parse_args()
 
     from gen import CONFIGS
@@ -169,6 +223,9 @@ def main():
                         seq_len=min(cfg.seq_len or T_, T_))
     if args.impl == "reference":
         run_reference(args, cfg)
+        return
+    if args.memory_curve:
+        run_memory_curve(args, cfg)
         return
     if args.warmup < 3:
         args.warmup = 3  # timing rule: at least three warm-up steps

@@ -41,11 +41,18 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kSmemMax = 232448;  // opt-in dynamic shared memory per block
 
 // Shared-memory plan of one CTA.  CG = CTAs per tile (1, or 2 for a CTA pair, where each
-// CTA holds 128 rows of A and half of the tile's B rows).
-template <int STAGING, int CG>
+// CTA holds 128 rows of A and half of the tile's B rows).  A pipeline stage holds KSUB
+// consecutive 64-deep k-blocks ("sub-blocks", each in the layout of one TMA box), so that
+// the per-stage costs (a barrier wait, a commit, the expect-tx) are paid once per KSUB
+// k-blocks; fewer, larger stages tolerate less memory latency, which the short launches of
+// the backward need, so the epilogue type chooses.
+template <int STAGING, int CG, int KSUB_>
 struct Shape {
-  static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = (kBNMax / CG) * BK * 2;
+  static constexpr int KSUB = KSUB_;
+  static constexpr int A_SUB = BM * BK * 2;
+  static constexpr int B_SUB = (kBNMax / CG) * BK * 2;
+  static constexpr int A_BYTES = KSUB * A_SUB;
+  static constexpr int B_BYTES = KSUB * B_SUB;
   static constexpr int STAGE = A_BYTES + B_BYTES;
   static constexpr int BAR_BYTES = 512;
   static constexpr int FIT = (kSmemMax - 1024 - BAR_BYTES - STAGING) / STAGE;
@@ -170,6 +177,7 @@ struct FwdEpi {
   Ctrl* ctrl;
 
   static constexpr int kStaging = 0;
+  static constexpr int kKSub = 2;
 
   __device__ __forceinline__ void run(uint32_t taddr, int m_t, int n_t, int r, int BN, const EpiCtx&,
                                       uint32_t&) const {
@@ -225,6 +233,7 @@ struct BwdEpi {
   __nv_bfloat16* G;
 
   static constexpr int kStaging = 0;
+  static constexpr int kKSub = 1;
 
   __device__ __forceinline__ void run(uint32_t taddr, int m_t, int n_t, int r, int BN, const EpiCtx&,
                                       uint32_t&) const {
@@ -290,6 +299,7 @@ struct F32Epi {
 
   static constexpr int kWarpStaging = 2 * 32 * 32 * 4;
   static constexpr int kStaging = 4 * kWarpStaging;
+  static constexpr int kKSub = 2;
 
   __device__ __forceinline__ void run(uint32_t taddr, int m_t, int n_t, int r, int bn, const EpiCtx& cx,
                                       uint32_t& seq) const {
@@ -365,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap tmO0, const __grid_constant__ CUtensorMap tmO1, Geom g,
                    Epi e0, Epi e1) {
   static_assert(CG == 1 || CG == 2, "one CTA or a CTA pair per tile");
-  using S = Shape<Epi::kStaging, CG>;
+  using S = Shape<Epi::kStaging, CG, (CG == 2 ? Epi::kKSub : 1)>;
   constexpr uint32_t IDESC = idesc_bf16_f32(BM * CG, 8, false, false) & ~(0x3Fu << 17);  // N set per problem
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -469,29 +479,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Prob q = tr.prob ? g.p[1] : g.p[0];
         const CUtensorMap* ta = tr.prob ? &tmA1 : &tmA0;
         const CUtensorMap* tb = tr.prob ? &tmB1 : &tmB0;
-        const uint32_t tx = static_cast<uint32_t>(CG * S::A_BYTES + q.bn * BK * 2);  // both CTAs' boxes
+        // bytes of one sub-block, both CTAs' boxes
+        const uint32_t tx_sub = static_cast<uint32_t>(CG * S::A_SUB + q.bn * BK * 2);
         const int m_row = (tr.m_t * CG + static_cast<int>(rank)) * BM;
         const int b_rows = q.bn / CG;
+        const int n_stages = (q.num_k + S::KSUB - 1) / S::KSUB;
         bool ok = true;
-        for (int kb = 0; kb < q.num_k; ++kb, ++it) {
+        for (int kb = 0; kb < n_stages; ++kb, ++it) {
           const int s = it % S::STAGES;
           const uint32_t ph = (it / S::STAGES) & 1;
           if (!wait_or_abort(&empty[s], ph ^ 1, af, ctrl)) {
             ok = false;
             break;
           }
-          if (leader) mbar_arrive_expect_tx(&full[s], tx);
+          const int nsub = q.num_k - kb * S::KSUB < S::KSUB ? q.num_k - kb * S::KSUB : S::KSUB;
+          if (leader) mbar_arrive_expect_tx(&full[s], tx_sub * static_cast<uint32_t>(nsub));
           uint8_t* a = sA + s * S::A_BYTES;
           uint8_t* b = sB + s * S::B_BYTES;
           if (CG == 2) {
             const uint32_t fb = full_leader0 + static_cast<uint32_t>(s) * 8u;
-            if (!q.a_mn) {
-              tma_load_2d_pair(a, ta, fb, kb * BK, m_row);
-            } else {
-              tma_load_2d_pair(a, ta, fb, m_row, kb * BK);
-              tma_load_2d_pair(a + 8192, ta, fb, m_row + 64, kb * BK);
+            for (int j = 0; j < nsub; ++j) {
+              const int kx = (kb * S::KSUB + j) * BK;
+              uint8_t* aj = a + j * S::A_SUB;
+              if (!q.a_mn) {
+                tma_load_2d_pair(aj, ta, fb, kx, m_row);
+              } else {
+                tma_load_2d_pair(aj, ta, fb, m_row, kx);
+                tma_load_2d_pair(aj + 8192, ta, fb, m_row + 64, kx);
+              }
+              tma_load_2d_pair(b + j * S::B_SUB, tb, fb, kx, tr.n_t * q.bn + static_cast<int>(rank) * b_rows);
             }
-            tma_load_2d_pair(b, tb, fb, kb * BK, tr.n_t * q.bn + static_cast<int>(rank) * b_rows);
           } else {
             if (!q.a_mn) {
               tma_load_2d(a, ta, &full[s], kb * BK, m_row);
@@ -533,8 +550,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_or_abort(&tempty[acc], (use & 1) ^ 1, af, ctrl)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * kBNMax;
+        // Descriptors of stage 0, sub-block 0; the others differ only in the start address
+        // field (address >> 4, which stays below 2^14 for any shared-memory offset), so
+        // the issue loop adds offsets instead of rebuilding them: one thread issues every
+        // MMA, and its instruction count per MMA shows up in the tensor pipe's duty cycle.
+        const uint64_t a_desc0 = q.a_mn ? sdesc_sw128(smem_u32(sA), 8192, 1024) : sdesc_sw128(smem_u32(sA), 16, 1024);
+        const uint64_t b_desc0 = q.b_mn ? sdesc_sw128(smem_u32(sB), 8192, 1024) : sdesc_sw128(smem_u32(sB), 16, 1024);
+        const uint64_t a_kstep = q.a_mn ? 2048 >> 4 : 32 >> 4, b_kstep = q.b_mn ? 2048 >> 4 : 32 >> 4;
+        const int n_stages = (q.num_k + S::KSUB - 1) / S::KSUB;
         bool ok = true;
-        for (int kb = 0; kb < q.num_k; ++kb, ++it) {
+        for (int kb = 0; kb < n_stages; ++kb, ++it) {
           const int s = it % S::STAGES;
           const uint32_t ph = (it / S::STAGES) & 1;
           if (!wait_or_abort(&full[s], ph, af, ctrl)) {
@@ -542,16 +567,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a_base = smem_u32(sA + s * S::A_BYTES);
-          const uint32_t b_base = smem_u32(sB + s * S::B_BYTES);
+          const int nsub = q.num_k - kb * S::KSUB < S::KSUB ? q.num_k - kb * S::KSUB : S::KSUB;
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {
-            const uint64_t ad =
-                q.a_mn ? sdesc_sw128(a_base + k * 2048, 8192, 1024) : sdesc_sw128(a_base + k * 32, 16, 1024);
-            const uint64_t bd =
-                q.b_mn ? sdesc_sw128(b_base + k * 2048, 8192, 1024) : sdesc_sw128(b_base + k * 32, 16, 1024);
-            if (CG == 2) umma_f16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0);
-            else umma_f16(d_tmem, ad, bd, idesc, (kb | k) != 0);
+          for (int j = 0; j < S::KSUB; ++j) {
+            if (j < nsub) {
+              const uint64_t ad = a_desc0 + static_cast<uint64_t>((s * S::A_BYTES + j * S::A_SUB) >> 4);
+              const uint64_t bd = b_desc0 + static_cast<uint64_t>((s * S::B_BYTES + j * S::B_SUB) >> 4);
+#pragma unroll
+              for (int k = 0; k < BK / 16; ++k) {
+                if (CG == 2) umma_f16_pair(d_tmem, ad + k * a_kstep, bd + k * b_kstep, idesc, (kb | j | k) != 0);
+                else umma_f16(d_tmem, ad + k * a_kstep, bd + k * b_kstep, idesc, (kb | j | k) != 0);
+              }
+            }
           }
           if (CG == 2) umma_commit_pair(&empty[s], 0x3);
           else umma_commit(&empty[s]);
@@ -650,7 +677,7 @@ struct KernelInfo {
 
 template <class Epi, int CG>
 cudaError_t kernel_units(int dev, int num_sms, int* units) {
-  using S = Shape<Epi::kStaging, CG>;
+  using S = Shape<Epi::kStaging, CG, (CG == 2 ? Epi::kKSub : 1)>;
   static KernelInfo info;
   auto kern = tc_gemm_kernel<Epi, CG>;
   const uint64_t bit = uint64_t(1) << (dev & 63);
@@ -688,7 +715,7 @@ cudaError_t kernel_units(int dev, int num_sms, int* units) {
 template <int CG, class Epi>
 cudaError_t launch_tc(const CUtensorMap* maps, const Prob* probs, int nprob, const Epi& e0, const Epi& e1,
                       TileSched* sched, int num_sms, cudaStream_t st) {
-  using S = Shape<Epi::kStaging, CG>;
+  using S = Shape<Epi::kStaging, CG, (CG == 2 ? Epi::kKSub : 1)>;
   static_assert(S::SMEM <= kSmemMax && S::STAGES >= 3, "shared memory budget");
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
