@@ -325,11 +325,13 @@ def main():
     tflops = flops / sec_per_step / 1e12
 
     # ---- roofline of the dominant kernel class (device time from its own events)
+    fused_bwd = per_class["grad_gemm"][0] == 0  # bf16: one launch per chunk runs G, dW and dH
+
     def class_flops(c):
         if c == "fwd_tiles":
             return 2.0 * d * V * T * args.steps
         if c == "bwd_tiles":
-            return 2.0 * d * V * n_valid * args.steps
+            return (6.0 if fused_bwd else 2.0) * d * V * n_valid * args.steps
         if c == "grad_gemm":
             return 4.0 * d * V * n_valid * args.steps
         return 0.0

@@ -17,21 +17,25 @@ namespace fckl {
 namespace {
 
 constexpr size_t kAlign = 256;
-// Budget of the gradient-tile stripe G[chunk, S]: small enough to stay in the 126 MB L2
-// while the dW and dH contractions read it back.
-constexpr size_t kStripeBudgetBytes = size_t(64) << 20;
+// Budget of the gradient stripes: small enough to stay in the 126 MB L2 while the dW and
+// dH contractions read them back.  The bf16 backward keeps three stripes G[chunk, S] in
+// flight (one being written, two being read); the f32 path one.
+constexpr size_t kStripeBudgetBytes = size_t(96) << 20;
+constexpr size_t kStripeBudgetBytesF32 = size_t(64) << 20;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct Sizes {
-  int64_t T, d, V, K, C, S, nvt;
+  int64_t T, d, V, K, C, S, nvt, stripes;
   size_t elem;  // bytes of one H / W / dH element
 };
 
 // The stripe width S of the backward (a multiple of 256 vocab columns).
-int64_t stripe_width(int64_t C, int64_t V, size_t g_elem) {
+int64_t stripe_width(int64_t C, int64_t V, size_t elem) {
   const int64_t vpad = (V + kTileV - 1) / kTileV * kTileV;
-  int64_t S = static_cast<int64_t>(kStripeBudgetBytes / (static_cast<size_t>(C) * g_elem));
+  const size_t per_col = elem == 2 ? static_cast<size_t>(C) * 2 * static_cast<size_t>(tc_grad_buffers())
+                                   : static_cast<size_t>(C) * 4;
+  int64_t S = static_cast<int64_t>((elem == 2 ? kStripeBudgetBytes : kStripeBudgetBytesF32) / per_col);
   S = S / kTileV * kTileV;
   if (S < kTileV) S = kTileV;
   if (S > vpad) S = vpad;
@@ -39,7 +43,7 @@ int64_t stripe_width(int64_t C, int64_t V, size_t g_elem) {
 }
 
 struct Layout {
-  size_t ctrl, row_loss, sidx, sp, slogp, zk, part, G, dHacc, HcT, total;
+  size_t ctrl, row_loss, sidx, sp, slogp, zk, part, G, done, dHacc, HcT, total;
   int64_t ldT;
 };
 
@@ -59,7 +63,9 @@ Layout layout_of(const Sizes& z) {
   L.slogp = take(4 * ck);
   L.zk = take(4 * ck);
   L.part = take(8 * static_cast<size_t>(z.C) * static_cast<size_t>(z.nvt));
-  L.G = take(static_cast<size_t>(z.C) * static_cast<size_t>(z.S) * (z.elem == 2 ? 2 : 4));
+  L.G = take(static_cast<size_t>(z.C) * static_cast<size_t>(z.S) *
+             (z.elem == 2 ? 2 * static_cast<size_t>(tc_grad_buffers()) : 4));
+  L.done = take(z.elem == 2 ? 2 * sizeof(unsigned int) * static_cast<size_t>(z.stripes) : 0);
   L.dHacc = take(z.elem == 2 ? 4 * static_cast<size_t>(z.C) * static_cast<size_t>(z.d) : 0);
   L.ldT = (z.C + 7) / 8 * 8;
   L.HcT = take(z.elem == 2 ? 2 * static_cast<size_t>(z.d) * static_cast<size_t>(L.ldT) : 0);
@@ -77,7 +83,8 @@ bool sizes_of(int64_t T, int64_t d, int64_t V, int32_t K, int64_t chunk, fckl_dt
   z->K = K;
   z->C = T == 0 ? 1 : (chunk < T ? chunk : T);
   z->elem = dt == FCKL_BF16 ? 2 : 4;
-  z->S = stripe_width(z->C, V, z->elem == 2 ? 2 : 4);
+  z->S = stripe_width(z->C, V, z->elem);
+  z->stripes = (V + z->S - 1) / z->S;
   z->nvt = (V + kTileV - 1) / kTileV;
   return true;
 }
@@ -122,6 +129,7 @@ ChunkScratch scratch_of(void* ws, const Layout& L) {
   s.zk = reinterpret_cast<float*>(b + L.zk);
   s.part = reinterpret_cast<float2*>(b + L.part);
   s.G = b + L.G;
+  s.done = reinterpret_cast<unsigned int*>(b + L.done);
   s.dHacc = reinterpret_cast<float*>(b + L.dHacc);
   s.HcT = b + L.HcT;
   s.ldT = L.ldT;
@@ -316,28 +324,25 @@ fckl_status fckl_backward(const void* H, const void* W, const int32_t* topk_idx,
       return launch_prep(topk_idx + c0 * K, topk_logits + c0 * K, rows, K, V, tau, s, ctrl, st);
     }));
     if (dtype == FCKL_BF16) {
+      // one launch for every stripe of the chunk (recomputed logits -> G -> dH, dW)
       const void* Hc = static_cast<const uint8_t*>(H) + c0 * d * 2;
       FCKL_TRY(step(FCKL_K_OTHER, st, [&] { return launch_transpose_bf16(Hc, rows, d, d, s.HcT, s.ldT, st); }));
+      FCKL_TRY(step(FCKL_K_OTHER, st,
+                    [&] { return cudaMemsetAsync(s.dHacc, 0, sizeof(float) * static_cast<size_t>(rows * d), st); }));
+      FCKL_TRY(step(FCKL_K_OTHER, st, [&] {
+        return cudaMemsetAsync(s.done, 0, 2 * sizeof(unsigned int) * static_cast<size_t>(z.stripes), st);
+      }));
+      FCKL_TRY(step(FCKL_K_BWD_TILES, st, [&] {
+        return tc_bwd_chunk(Hc, s.HcT, s.ldT, W, rows, d, V, S, tau, s.sidx, s.sp, K, lse + c0, valid + c0, ctrl,
+                            s.G, dW, c0 > 0, s.dHacc, s.done, s.done + z.stripes, &sched, num_sms, st);
+      }));
+      void* out = static_cast<uint8_t*>(dH) + c0 * d * 2;
+      FCKL_TRY(step(FCKL_K_OTHER, st, [&] { return launch_f32_to_bf16(s.dHacc, out, rows * d, st); }));
+      continue;
     }
     for (int64_t s0 = 0; s0 < V; s0 += S) {
       const int64_t s_eff = (V - s0 < S) ? V - s0 : S;
-      const bool last = s0 + S >= V;
-      if (dtype == FCKL_BF16) {
-        const void* Hc = static_cast<const uint8_t*>(H) + c0 * d * 2;
-        const void* Ws = static_cast<const uint8_t*>(W) + s0 * d * 2;
-        FCKL_TRY(step(FCKL_K_BWD_TILES, st, [&] {
-          return tc_bwd_tiles(Hc, W, rows, d, V, s0, S, tau, s.sidx, s.sp, K, lse + c0, valid + c0, ctrl, s.G, S,
-                              &sched, num_sms, st);
-        }));
-        FCKL_TRY(step(FCKL_K_GRAD_GEMM, st, [&] {
-          return tc_dW_dH(s.G, S, s.HcT, s.ldT, Ws, rows, d, s_eff, dW + s0 * d, c0 > 0, s.dHacc, s0 > 0, ctrl, &sched,
-                          num_sms, st);
-        }));
-        if (last) {
-          void* out = static_cast<uint8_t*>(dH) + c0 * d * 2;
-          FCKL_TRY(step(FCKL_K_OTHER, st, [&] { return launch_f32_to_bf16(s.dHacc, out, rows * d, st); }));
-        }
-      } else {
+      {
         const float* Hc = static_cast<const float*>(H) + c0 * d;
         const float* Wf = static_cast<const float*>(W);
         float* G = static_cast<float*>(s.G);

@@ -45,7 +45,8 @@ struct ChunkScratch {
   float* slogp;     // [C, K] teacher log p, permuted like sidx
   float* zk;        // [C, K] student logit at sidx (forward)
   float2* part;     // [C, nvt] per (row, 256-wide vocab tile): (max, sum) in log2 units
-  void* G;          // [C, S] gradient tile stripe (bf16 for bf16 work, f32 for f32 work)
+  void* G;          // gradient stripes: [C, 3 S] bf16 (bf16 work) or [C, S] f32 (f32 work)
+  unsigned int* done;  // [2, stripes] completion counters of the chunk backward (bf16 work)
   float* dHacc;     // [C, d] fp32 dH accumulator (bf16 work only)
   void* HcT;        // [d, ldT] bf16 transposed hidden states of the chunk (bf16 work only)
   int64_t ldT;      // C rounded up to a multiple of 8
@@ -83,18 +84,20 @@ cudaError_t launch_simt_gemm(const float* A, int64_t sam, int64_t sak, const flo
 cudaError_t tc_fwd_tiles(const void* Hc, const void* W, int64_t rows, int64_t d, int64_t V,
                          float tau, const int32_t* sidx, int32_t K, float* zk, float2* part, int nvt,
                          Ctrl* ctrl, TileSched* sched, int num_sms, cudaStream_t st);
-cudaError_t tc_bwd_tiles(const void* Hc, const void* W, int64_t rows, int64_t d, int64_t V,
-                         int64_t s0, int64_t S, float tau, const int32_t* sidx, const float* sp,
-                         int32_t K, const float* lse, const uint8_t* valid, Ctrl* ctrl,
-                         void* G, int64_t ldG, TileSched* sched, int num_sms, cudaStream_t st);
-// One launch for both contractions of a (chunk, stripe) step, G being [rows, ldG] bf16 with
-// its first S columns used and HcT the chunk's hidden states transposed, [d, ldT] bf16:
-//   dH accumulator acc[rows, d] (+)= G . W[s0:s0+S, :]
-//   dW[s0:s0+S, :] (+)= G^T . Hc
-cudaError_t tc_dW_dH(const void* G, int64_t ldG, const void* HcT, int64_t ldT, const void* W_stripe,
-                     int64_t rows, int64_t d, int64_t S, float* dW_stripe, int dW_accumulate,
-                     float* dH_acc, int dH_accumulate, Ctrl* ctrl, TileSched* sched, int num_sms,
-                     cudaStream_t st);
+// Gradient buffers the chunk backward rotates through (each [rows, S] bf16, side by side).
+int tc_grad_buffers();
+// The whole backward of one chunk in one launch, over every vocab stripe of width S:
+//   G_s = (softmax - p) * g / (tau N) of the recomputed logit tile H_chunk . W_s^T (bf16)
+//   dH accumulator acc[rows, d] += G_s . W_s            (acc must hold zeros at entry)
+//   dW[s*S:(s+1)*S, :] (+)= G_s^T . H_chunk             (stored when !dW_accumulate)
+// G is [rows, 3 S] bf16 (three rotating stripe buffers); HcT is H_chunk transposed, [d, ldT]
+// bf16; done_g / done_w are [ceil(V / S)] completion counters that must hold zeros at entry.
+cudaError_t tc_bwd_chunk(const void* Hc, const void* HcT, int64_t ldT, const void* W, int64_t rows,
+                         int64_t d, int64_t V, int64_t S, float tau, const int32_t* sidx,
+                         const float* sp, int32_t K, const float* lse, const uint8_t* valid,
+                         Ctrl* ctrl, void* G, float* dW, int dW_accumulate, float* dH_acc,
+                         unsigned int* done_g, unsigned int* done_w, TileSched* sched, int num_sms,
+                         cudaStream_t st);
 cudaError_t tc_debug_gemm(const void* A, const void* B, float* D, int64_t M, int64_t N, int64_t K,
                           int a_mn, int b_mn, int cta_pair, int num_sms, cudaStream_t st);
 

@@ -18,12 +18,14 @@
 //   BwdEpi   recomputed logit tile -> G = (softmax - p_teacher) * g / (tau N) in bf16;
 //   F32Epi   fp32 tile -> TMA store or TMA reduce-add (dW, dH and the engine's test hook),
 //            optionally transposed.
+// The backward of one chunk is a single launch over every vocab stripe: G tiles, dH^T
+// tiles and dW tiles of all stripes in one tile sequence, ordered by dependency and
+// synchronized through per-stripe completion counters (see BwdChunkEpi).
 #include <cuda_bf16.h>
 
 #include <atomic>
 #include <cfloat>
 #include <climits>
-#include <initializer_list>
 
 #include "fckl_internal.h"
 #include "fckl_ptx.cuh"
@@ -36,16 +38,18 @@ constexpr int BK = 64;            // one 128-byte swizzle row of bf16
 constexpr int kBNMax = 256;       // widest tile (N) of any problem
 constexpr int kThreads = 192;     // 6 warps
 constexpr int kEpiThreads = 128;  // warps 2..5
+constexpr int kEpiWarps = kEpiThreads / 32;
 constexpr int kTmemCols = 512;    // two accumulators of up to 256 fp32 columns
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kSmemMax = 232448;  // opt-in dynamic shared memory per block
+constexpr int kMaxProb = 3;
 
 // Shared-memory plan of one CTA.  CG = CTAs per tile (1, or 2 for a CTA pair, where each
 // CTA holds 128 rows of A and half of the tile's B rows).  A pipeline stage holds KSUB
 // consecutive 64-deep k-blocks ("sub-blocks", each in the layout of one TMA box), so that
 // the per-stage costs (a barrier wait, a commit, the expect-tx) are paid once per KSUB
-// k-blocks; fewer, larger stages tolerate less memory latency, which the short launches of
-// the backward need, so the epilogue type chooses.
+// k-blocks; fewer, larger stages tolerate less memory latency, so the epilogue type
+// chooses.
 template <int STAGING, int CG, int KSUB_>
 struct Shape {
   static constexpr int KSUB = KSUB_;
@@ -60,6 +64,13 @@ struct Shape {
   static constexpr int SMEM = 1024 + STAGES * STAGE + STAGING + BAR_BYTES;
 };
 
+// The tensor maps of a launch: per problem an A and a B operand map and an output map
+// (fp32 TMA epilogues).  Passed as one __grid_constant__ kernel parameter, so each map
+// lives in parameter space where TMA may read it.
+struct Maps {
+  CUtensorMap a[kMaxProb], b[kMaxProb], o[kMaxProb];
+};
+
 // What the engine hands every epilogue besides its TMEM address: the output tensor map
 // of the tile's problem (TMA epilogues) and this CTA's staging shared memory.
 struct EpiCtx {
@@ -67,7 +78,7 @@ struct EpiCtx {
   uint8_t* staging;
 };
 
-// One GEMM problem of a launch: D[M, N] = A . B over K, tiled 128 x bn x 64.
+// One GEMM problem of a launch: D[M, N] = A . B over K, tiled (128 * CG) x bn x 64.
 struct Prob {
   int num_m, num_n, num_k;
   int tiles;       // num_m * num_n
@@ -76,36 +87,96 @@ struct Prob {
   int bn;          // tile width: a multiple of 32 (of 64 for an MN-major B), at most 256
 };
 
-// A launch: one or two problems (tiles of the second follow those of the first), and the
-// dynamic tile counter (a word in the workspace that reads `base` when the launch starts),
-// or none for static round-robin scheduling.
+// A launch: up to three problems and the dynamic tile counter (a word in the workspace
+// that reads `base` when the launch starts), or none for static round-robin scheduling.
+// Plain launches run the tiles of problem 0, then of 1, then of 2.  A chunk backward
+// (`stripes` > 0) runs, for every vocab stripe s of width S, the G tiles (problem 0), the
+// dH^T tiles (1) and the dW tiles (2) of that stripe, in the order
+//   G(0), G(1), grad(0), G(2), grad(1), ..., G(ns-1), grad(ns-2), grad(ns-1)
+// (grad = the dH^T and dW tiles), G(s) writing gradient buffer s % 3; see BwdChunkEpi.
 struct Geom {
-  Prob p[2];
+  Prob p[kMaxProb];
   int nprob;
   int tiles;
   unsigned int* counter;
   unsigned int base;
+  int stripes;          // 0 for a plain launch
+  int S;                // stripe width (vocab columns; a multiple of 256)
+  int last_cols;        // vocab columns of the last stripe
+  unsigned int* done_g; // [stripes]: finished G tiles (each CTA of a pair adds one)
+  unsigned int* done_w; // [stripes]: finished dH^T and dW tiles
 };
 
+constexpr int kGradBuffers = 3;
+
+// A tile: its problem, vocab stripe (chunk backward), position, depth and the coordinate
+// offsets of its operands (k: along K; m / n: along the operand's M / N rows).
 struct TileRef {
-  int prob, m_t, n_t;
+  int prob, stripe, m_t, n_t, num_k;
+  int a_k_off, a_m_off, b_k_off, b_n_off;
+  int skip;  // entirely outside the vocabulary (chunk backward's last stripe): no work
 };
 
-__device__ __forceinline__ TileRef tile_of(const Geom& g, int t) {
-  int p = 0;
-  if (g.nprob > 1 && t >= g.p[0].tiles) {
-    t -= g.p[0].tiles;
-    p = 1;
-  }
-  const Prob q = p ? g.p[1] : g.p[0];
-  TileRef r;
-  r.prob = p;
+__device__ __forceinline__ void raster(const Prob& q, int t, int& m_t, int& n_t) {
   if (q.n_fastest) {
-    r.n_t = t % q.num_n;
-    r.m_t = t / q.num_n;
+    n_t = t % q.num_n;
+    m_t = t / q.num_n;
   } else {
-    r.m_t = t % q.num_m;
-    r.n_t = t / q.num_m;
+    m_t = t % q.num_m;
+    n_t = t / q.num_m;
+  }
+}
+
+template <int CG>
+__device__ __forceinline__ TileRef tile_of(const Geom& g, int t) {
+  TileRef r{};
+  if (!g.stripes) {
+    int p = 0;
+    while (p + 1 < g.nprob && t >= g.p[p].tiles) t -= g.p[p++].tiles;
+    r.prob = p;
+    raster(g.p[p], t, r.m_t, r.n_t);
+    r.num_k = g.p[p].num_k;
+    return r;
+  }
+  const int nG = g.p[0].tiles, nR = g.p[1].tiles + g.p[2].tiles, ns = g.stripes;
+  int s, local, grad;
+  if (t < nG) {
+    s = 0, local = t, grad = 0;
+  } else {
+    const int u = (t - nG) / (nG + nR);
+    if (u < ns - 1) {
+      const int rr = t - nG - u * (nG + nR);
+      grad = rr >= nG;
+      s = grad ? u : u + 1;
+      local = grad ? rr - nG : rr;
+    } else {
+      s = ns - 1, grad = 1, local = t - nG - (ns - 1) * (nG + nR);
+    }
+  }
+  const int cols = s == ns - 1 ? g.last_cols : g.S;
+  const int buf = s % kGradBuffers;
+  r.stripe = s;
+  if (!grad) {
+    // G[rows, S-stripe] = H_chunk . W_s^T: B rows are vocab rows s*S + n
+    r.prob = 0;
+    raster(g.p[0], local, r.m_t, r.n_t);
+    r.num_k = g.p[0].num_k;
+    r.b_n_off = s * g.S;
+    r.skip = r.n_t * g.p[0].bn >= cols;
+  } else if (local < g.p[1].tiles) {
+    // dH^T[d, rows] += W_s^T . G^T: A = W rows (K) s*S.., B = G buffer columns (K) buf*S..
+    r.prob = 1;
+    raster(g.p[1], local, r.m_t, r.n_t);
+    r.num_k = (cols + BK - 1) / BK;
+    r.a_k_off = s * g.S;
+    r.b_k_off = buf * g.S;
+  } else {
+    // dW[s*S + m, d] (+)= G^T . H_chunk: A = G buffer columns (M) buf*S..
+    r.prob = 2;
+    raster(g.p[2], local - g.p[1].tiles, r.m_t, r.n_t);
+    r.num_k = g.p[2].num_k;
+    r.a_m_off = buf * g.S;
+    r.skip = r.m_t * BM * CG >= cols;
   }
   return r;
 }
@@ -142,6 +213,26 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, co
   }
 }
 
+// Waits until a completion counter written by other CTAs reaches `target` (acquire), with
+// the same bound and abort protocol as the mbarrier waits.
+__device__ __forceinline__ bool wait_counter(const unsigned int* c, unsigned int target, const AbortFlag& af,
+                                             Ctrl* ctrl) {
+  if (ld_acquire_gpu(c) >= target) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 0;; ++i) {
+    __nanosleep(128);
+    if (ld_acquire_gpu(c) >= target) return true;
+    if ((i & 15) == 15) {
+      if (*af.local) return false;
+      if (global_ns() - t0 > FCKL_WAIT_NS) {
+        af.raise();
+        if (ctrl) set_status(ctrl, FCKL_ERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
 __device__ __forceinline__ int lower_bound_ids(const int32_t* ids, int K, int64_t lo) {
   int a = 0, b = K;
   while (a < b) {
@@ -160,9 +251,12 @@ __device__ __forceinline__ float pick32(const uint32_t (&v)[32], int j) {
 
 // ----------------------------------------------------------------------------------------
 // Epilogues.  run() is called by every epilogue thread for every tile; `taddr` addresses
-// the thread's TMEM lane (tile row r) at the accumulator's first column.  tcgen05.ld is
-// warp-collective, so loops over columns are uniform across the warp and only the
-// memory traffic is predicated on the row.
+// the thread's TMEM lane (tile row r) at the accumulator's first column and m_blk is the
+// 128-row block of the result that this CTA holds.  tcgen05.ld is warp-collective, so
+// loops over columns are uniform across the warp and only the memory traffic is predicated
+// on the row.  done() is called once per tile by one epilogue thread after all four
+// epilogue warps of the CTA have finished it (only when kSignals), with their global
+// stores fenced at GPU scope and toward the async proxy.
 
 // Forward logit tile (256 vocab columns): per-row (max, sum) of exp2(z * log2e / tau)
 // over the tile's columns, and z at every teacher id that falls in the tile.
@@ -178,11 +272,13 @@ struct FwdEpi {
 
   static constexpr int kStaging = 0;
   static constexpr int kKSub = 2;
+  static constexpr bool kSignals = false;
 
-  __device__ __forceinline__ void run(uint32_t taddr, int m_t, int n_t, int r, int BN, const EpiCtx&,
+  __device__ __forceinline__ void run(const TileRef& tr, uint32_t taddr, int m_blk, int r, int BN, const EpiCtx&,
                                       uint32_t&) const {
-    const int64_t row = static_cast<int64_t>(m_t) * BM + r;
+    const int64_t row = static_cast<int64_t>(m_blk) * BM + r;
     const bool live = row < rows;
+    const int n_t = tr.n_t;
     const int64_t n0 = static_cast<int64_t>(n_t) * BN;
     const int32_t* ids = sidx + (live ? row : 0) * K;
     int k = live ? lower_bound_ids(ids, K, n0) : K;
@@ -217,12 +313,16 @@ struct FwdEpi {
     }
     if (live) part[row * nvt + n_t] = make_float2(m_run, s_run);
   }
+
+  __device__ __forceinline__ void done(const TileRef&) const {}
 };
 
-// Backward logit tile of a vocab stripe [s0, s0 + S): G = (exp(s - lse) - p) * alpha,
-// alpha = g / (tau N) for valid rows and 0 for ignored rows, stored as bf16 [rows, ldG].
+// Backward logit tile of vocab stripe s (columns [s0, s0 + S) with s0 = s * S):
+// G = (exp(s - lse) - p) * alpha, alpha = g / (tau N) for valid rows and 0 for ignored
+// rows, stored as bf16 into gradient buffer s % 3 (columns [buf * S, buf * S + S) of the
+// [rows, ldG] buffer, ldG = 3 * S).  Columns at or past V are written as zeros.
 struct BwdEpi {
-  int64_t rows, V, s0, S, ldG;
+  int64_t rows, V, S, ldG;
   float c2;
   const int32_t* sidx;
   const float* sp;
@@ -232,16 +332,15 @@ struct BwdEpi {
   Ctrl* ctrl;
   __nv_bfloat16* G;
 
-  static constexpr int kStaging = 0;
-  static constexpr int kKSub = 1;
-
-  __device__ __forceinline__ void run(uint32_t taddr, int m_t, int n_t, int r, int BN, const EpiCtx&,
-                                      uint32_t&) const {
-    const int64_t row = static_cast<int64_t>(m_t) * BM + r;
+  __device__ __forceinline__ void run(const TileRef& tr, uint32_t taddr, int m_blk, int r, int BN,
+                                      const EpiCtx&, uint32_t&) const {
+    const int64_t row = static_cast<int64_t>(m_blk) * BM + r;
     const bool live = row < rows;
-    const int64_t n0l = static_cast<int64_t>(n_t) * BN;
+    const int64_t s0 = static_cast<int64_t>(tr.stripe) * S;
+    const int64_t n0l = static_cast<int64_t>(tr.n_t) * BN;
     const int64_t n0 = s0 + n0l;
     const int64_t vend = (s0 + S < V) ? s0 + S : V;
+    __nv_bfloat16* Gb = G + (tr.stripe % kGradBuffers) * S;
     float lse2 = 0.f, a = 0.f;
     const int32_t* ids = sidx + (live ? row : 0) * K;
     int k = K;
@@ -276,7 +375,7 @@ struct BwdEpi {
           __nv_bfloat162 h = __floats2bfloat162_rn(g[2 * i] * a, g[2 * i + 1] * a);
           w[i] = *reinterpret_cast<uint32_t*>(&h);
         }
-        uint4* dst = reinterpret_cast<uint4*>(G + row * ldG + n0l + c);
+        uint4* dst = reinterpret_cast<uint4*>(Gb + row * ldG + n0l + c);
 #pragma unroll
         for (int q = 0; q < 4; ++q) dst[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
       }
@@ -288,25 +387,29 @@ struct BwdEpi {
 // 32-column chunk it writes a 32 x 32 fp32 block into one of its two 4 KB staging buffers
 // (128-byte swizzle: rows of 128 bytes whose 16-byte pieces are permuted by row % 8, so a
 // warp's stores hit distinct banks) and one lane issues a TMA reduce-add into the output
-// (accumulate) or a TMA store (first pass).  The read-modify-write happens in L2 and the
-// epilogue never waits on HBM.  With `transpose`, D[m, n] goes to out[n][m]: the block is
-// written transposed into the buffer and stored at (x = m, y = n).  The output map has a
-// 32 x 32 box and clips everything outside the M x N result.
+// (accumulate) or a TMA store.  The read-modify-write happens in L2 and the epilogue never
+// waits on HBM.  With `transpose`, D[m, n] goes to out[n][m]: the block is written
+// transposed into the buffer and stored at (x = m, y = n).  The output map has a 32 x 32
+// box and clips everything outside the result; y_stripe shifts the rows of a chunk
+// backward's dW tile to its vocab stripe.
 struct F32Epi {
   int64_t M, N;  // of D
   int accumulate, transpose;
+  int64_t y_stripe;  // rows of the output per vocab stripe (0: no shift)
   Ctrl* ctrl;
 
   static constexpr int kWarpStaging = 2 * 32 * 32 * 4;
   static constexpr int kStaging = 4 * kWarpStaging;
   static constexpr int kKSub = 2;
+  static constexpr bool kSignals = false;
 
-  __device__ __forceinline__ void run(uint32_t taddr, int m_t, int n_t, int r, int bn, const EpiCtx& cx,
-                                      uint32_t& seq) const {
+  __device__ __forceinline__ void run(const TileRef& tr, uint32_t taddr, int m_blk, int r, int bn,
+                                      const EpiCtx& cx, uint32_t& seq) const {
     const int lane = r & 31, quad = r >> 5;
     uint8_t* wbuf = cx.staging + quad * kWarpStaging;
-    const int64_t n0 = static_cast<int64_t>(n_t) * bn;
-    const int64_t m0 = static_cast<int64_t>(m_t) * BM + quad * 32;
+    const int64_t n0 = static_cast<int64_t>(tr.n_t) * bn;
+    const int64_t m0 = static_cast<int64_t>(m_blk) * BM + quad * 32;
+    const int64_t y0 = static_cast<int64_t>(tr.stripe) * y_stripe;
 #pragma unroll 1
     for (int c = 0; c < bn; c += 32) {
       if (n0 + c >= N) break;
@@ -334,11 +437,54 @@ struct F32Epi {
       __syncwarp();
       if (lane == 0 && m0 < M) {
         const int32_t x = static_cast<int32_t>(transpose ? m0 : n0 + c);
-        const int32_t y = static_cast<int32_t>(transpose ? n0 + c : m0);
+        const int32_t y = static_cast<int32_t>(transpose ? n0 + c : y0 + m0);
         if (accumulate) tma_reduce_add_2d(cx.out, buf, x, y);
         else tma_store_2d(cx.out, buf, x, y);
         bulk_commit();
       }
+    }
+  }
+
+  __device__ __forceinline__ void done(const TileRef&) const {}
+};
+
+// The backward of one chunk in one launch: problem 0 = G tiles (BwdEpi), 1 = dH^T tiles
+// (F32Epi, transposed, reduce-added into the chunk's fp32 dH accumulator, which starts at
+// zero), 2 = dW tiles (F32Epi, stored on the first chunk, reduce-added after).  Gradient
+// stripes rotate through three buffers.  Two kinds of dependency, both on tiles that come
+// earlier in the tile order, so a persistent grid always makes progress:
+//   a dH^T or dW tile of stripe s reads G(s): it waits for all G tiles of stripe s;
+//   a G tile of stripe s >= 3 overwrites the buffer of stripe s - 3: it waits for all
+//   dH^T and dW tiles of stripe s - 3.
+// The producers of both CTAs of a pair wait on the counters (acquire, then a proxy fence
+// so that their TMA reads see the G written by other CTAs' plain stores); each CTA adds
+// one to its stripe's counter when its epilogue has finished a tile (release, after a
+// proxy fence).
+struct BwdChunkEpi {
+  BwdEpi g;
+  F32Epi h, w;
+  Ctrl* ctrl;
+  unsigned int* done_g;
+  unsigned int* done_w;
+
+  static constexpr int kStaging = F32Epi::kStaging;
+  static constexpr int kKSub = 1;
+  static constexpr bool kSignals = true;
+
+  __device__ __forceinline__ void run(const TileRef& tr, uint32_t taddr, int m_blk, int r, int bn,
+                                      const EpiCtx& cx, uint32_t& seq) const {
+    if (tr.prob == 0) g.run(tr, taddr, m_blk, r, bn, cx, seq);
+    else if (tr.prob == 1) h.run(tr, taddr, m_blk, r, bn, cx, seq);
+    else w.run(tr, taddr, m_blk, r, bn, cx, seq);
+  }
+
+  __device__ __forceinline__ void done(const TileRef& tr) const {
+    __threadfence();
+    if (tr.prob == 0) {
+      fence_proxy_async_global();
+      atomicAdd(&done_g[tr.stripe], 1u);
+    } else {
+      atomicAdd(&done_w[tr.stripe], 1u);
     }
   }
 };
@@ -346,7 +492,7 @@ struct F32Epi {
 // ----------------------------------------------------------------------------------------
 // The engine.  Per problem, a_mn / b_mn select the operand layouts:
 //   A K-major: A[m, k] at row m of a [M, K] tensor (TMA box 64 x 128);
-//   A MN-major: A[m, k] at row k of a [K, M] tensor (two 64 x 64 boxes per stage);
+//   A MN-major: A[m, k] at row k of a [K, M] tensor (two 64 x 64 boxes per sub-block);
 //   B K-major: B[n, k] at row n of a [N, K] tensor (box 64 x bn/CG), so D = A . B^T;
 //   B MN-major: B[k, n] at row k of a [K, N] tensor (bn/64 boxes of 64 x 64; CG = 1 only).
 // (On this part an MN-major B operand costs 12-25% of MMA throughput and an MN-major A
@@ -357,23 +503,21 @@ struct F32Epi {
 // B, and the leader (rank 0) issues cta_group::2 MMAs that read both CTAs' shared memory
 // and write each CTA's 128 accumulator rows into its own TMEM.  Per SM, a 64-deep k-block
 // then costs 32 KB of operand traffic instead of 48 KB for the same 128 x 256 x 64 MMA
-// work, which is what the L2 -> SM path can sustain.  Both CTAs' loads signal the leader's
-// `full` barrier; the leader's commits arrive on both CTAs' `empty` and `tfull` barriers;
-// the peer's epilogue warps release accumulators on the leader's `tempty` barrier.
+// work.  Both CTAs' loads signal the leader's `full` barrier; the leader's commits arrive
+// on both CTAs' `empty` and `tfull` barriers; the peer's epilogue warps release
+// accumulators on the leader's `tempty` barrier.
 //
 // Tiles are handed out by the (leader's) producer warp: from the global counter when
 // there is one (each CTA or pair takes the next tile when it is ready for one, which
 // balances tiles of different cost), else round-robin; the tile sequence reaches the MMA
-// warp and the epilogue warps of both CTAs through a small shared-memory queue.
+// warp and the epilogue warps of both CTAs through a small shared-memory queue.  Tiles
+// marked `skip` never enter the queue: the leader counts them as done for the
+// dependency counters and moves on.
 constexpr int kQueue = 4;
-constexpr int kEpiWarps = kEpiThreads / 32;
 
 template <class Epi, int CG>
 __global__ void __launch_bounds__(kThreads, 1)
-    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmB0,
-                   const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
-                   const __grid_constant__ CUtensorMap tmO0, const __grid_constant__ CUtensorMap tmO1, Geom g,
-                   Epi e0, Epi e1) {
+    tc_gemm_kernel(const __grid_constant__ Maps maps, const Geom g, const Epi epi) {
   static_assert(CG == 1 || CG == 2, "one CTA or a CTA pair per tile");
   using S = Shape<Epi::kStaging, CG, (CG == 2 ? Epi::kKSub : 1)>;
   constexpr uint32_t IDESC = idesc_bf16_f32(BM * CG, 8, false, false) & ~(0x3Fu << 17);  // N set per problem
@@ -391,6 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* tileq = reinterpret_cast<int*>(qempty + kQueue);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tileq + kQueue);
   volatile int* abort_local = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint32_t* epi_count = tmem_slot + 2;  // [2]: epilogue warps through the tiles of each accumulator
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;
@@ -401,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto remote = [&](const void* p, uint32_t r) { return mapa_shared(smem_u32(p), r); };
   const AbortFlag af{abort_local, CG == 2 ? remote(const_cast<int*>(abort_local), rank ^ 1u) : 0u};
 
-  Ctrl* ctrl = e0.ctrl;
+  Ctrl* ctrl = epi.ctrl;
   if (threadIdx.x == 0) {
     for (int s = 0; s < S::STAGES; ++s) {
       mbar_init(&full[s], 1);
@@ -418,17 +563,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&qempty[q], 1 + CG * kEpiWarps + (CG - 1));
     }
     *abort_local = 0;
+    epi_count[0] = epi_count[1] = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tmA0);
-    tma_prefetch_desc(&tmB0);
-    if (Epi::kStaging) tma_prefetch_desc(&tmO0);
-    if (g.nprob > 1) {
-      tma_prefetch_desc(&tmA1);
-      tma_prefetch_desc(&tmB1);
-      if (Epi::kStaging) tma_prefetch_desc(&tmO1);
+    for (int p = 0; p < g.nprob; ++p) {
+      tma_prefetch_desc(&maps.a[p]);
+      tma_prefetch_desc(&maps.b[p]);
+      if (Epi::kStaging) tma_prefetch_desc(&maps.o[p]);
     }
   }
   if (warp == 1) {
@@ -450,19 +593,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t it = 0;
       int next_static = unit;
       const uint32_t full_leader0 = CG == 2 ? remote(&full[0], 0) : 0u;
+      const unsigned int g_target = static_cast<unsigned int>(CG * g.p[0].tiles);
+      const unsigned int w_target = static_cast<unsigned int>(CG * (g.p[1].tiles + g.p[2].tiles));
       for (int i = 0;; ++i) {
         const int slot = i % kQueue;
         const uint32_t qph = (i / kQueue) & 1;
         int t;
+        TileRef tr{};
         if (leader) {
           if (!wait_or_abort(&qempty[slot], qph ^ 1, af, ctrl)) break;
-          if (g.counter) {
-            t = static_cast<int>(atomicAdd(g.counter, 1u) - g.base);
-          } else {
-            t = next_static;
-            next_static += units;
+          for (;;) {
+            if (g.counter) {
+              t = static_cast<int>(atomicAdd(g.counter, 1u) - g.base);
+            } else {
+              t = next_static;
+              next_static += units;
+            }
+            if (t >= g.tiles) {
+              t = -1;
+              break;
+            }
+            tr = tile_of<CG>(g, t);
+            if (!tr.skip) break;
+            // nothing to compute: count it for both CTAs of the pair
+            atomicAdd(tr.prob == 0 ? &g.done_g[tr.stripe] : &g.done_w[tr.stripe], static_cast<unsigned int>(CG));
           }
-          if (t >= g.tiles) t = -1;
           tileq[slot] = t;
           mbar_arrive(&qfull[slot]);
           if (CG == 2) {
@@ -473,17 +628,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!wait_or_abort<true>(&qfull[slot], qph, af, ctrl)) break;
           t = tileq[slot];
           mbar_arrive_cluster(remote(&qempty[slot], 0));
+          if (t >= 0) tr = tile_of<CG>(g, t);
         }
         if (t < 0) break;
-        const TileRef tr = tile_of(g, t);
-        const Prob q = tr.prob ? g.p[1] : g.p[0];
-        const CUtensorMap* ta = tr.prob ? &tmA1 : &tmA0;
-        const CUtensorMap* tb = tr.prob ? &tmB1 : &tmB0;
+        if (g.stripes) {
+          // chunk backward: the tile's inputs (G of its stripe) or its output buffer (the
+          // stripe three back) must be ready
+          bool ok = true;
+          if (tr.prob != 0) ok = wait_counter(&g.done_g[tr.stripe], g_target, af, ctrl);
+          else if (tr.stripe >= kGradBuffers)
+            ok = wait_counter(&g.done_w[tr.stripe - kGradBuffers], w_target, af, ctrl);
+          if (!ok) break;
+          fence_proxy_async_global();
+        }
+        const Prob q = g.p[tr.prob];
+        const CUtensorMap* ta = &maps.a[tr.prob];
+        const CUtensorMap* tb = &maps.b[tr.prob];
         // bytes of one sub-block, both CTAs' boxes
         const uint32_t tx_sub = static_cast<uint32_t>(CG * S::A_SUB + q.bn * BK * 2);
-        const int m_row = (tr.m_t * CG + static_cast<int>(rank)) * BM;
+        const int m_row = (tr.m_t * CG + static_cast<int>(rank)) * BM + tr.a_m_off;
         const int b_rows = q.bn / CG;
-        const int n_stages = (q.num_k + S::KSUB - 1) / S::KSUB;
+        const int n_row = tr.n_t * q.bn + static_cast<int>(rank) * b_rows + tr.b_n_off;
+        const int n_stages = (tr.num_k + S::KSUB - 1) / S::KSUB;
         bool ok = true;
         for (int kb = 0; kb < n_stages; ++kb, ++it) {
           const int s = it % S::STAGES;
@@ -492,7 +658,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          const int nsub = q.num_k - kb * S::KSUB < S::KSUB ? q.num_k - kb * S::KSUB : S::KSUB;
+          const int nsub = tr.num_k - kb * S::KSUB < S::KSUB ? tr.num_k - kb * S::KSUB : S::KSUB;
           if (leader) mbar_arrive_expect_tx(&full[s], tx_sub * static_cast<uint32_t>(nsub));
           uint8_t* a = sA + s * S::A_BYTES;
           uint8_t* b = sB + s * S::B_BYTES;
@@ -502,25 +668,25 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int kx = (kb * S::KSUB + j) * BK;
               uint8_t* aj = a + j * S::A_SUB;
               if (!q.a_mn) {
-                tma_load_2d_pair(aj, ta, fb, kx, m_row);
+                tma_load_2d_pair(aj, ta, fb, kx + tr.a_k_off, m_row);
               } else {
-                tma_load_2d_pair(aj, ta, fb, m_row, kx);
-                tma_load_2d_pair(aj + 8192, ta, fb, m_row + 64, kx);
+                tma_load_2d_pair(aj, ta, fb, m_row, kx + tr.a_k_off);
+                tma_load_2d_pair(aj + 8192, ta, fb, m_row + 64, kx + tr.a_k_off);
               }
-              tma_load_2d_pair(b + j * S::B_SUB, tb, fb, kx, tr.n_t * q.bn + static_cast<int>(rank) * b_rows);
+              tma_load_2d_pair(b + j * S::B_SUB, tb, fb, kx + tr.b_k_off, n_row);
             }
           } else {
+            const int kx = kb * BK;
             if (!q.a_mn) {
-              tma_load_2d(a, ta, &full[s], kb * BK, m_row);
+              tma_load_2d(a, ta, &full[s], kx + tr.a_k_off, m_row);
             } else {
-              tma_load_2d(a, ta, &full[s], m_row, kb * BK);
-              tma_load_2d(a + 8192, ta, &full[s], m_row + 64, kb * BK);
+              tma_load_2d(a, ta, &full[s], m_row, kx + tr.a_k_off);
+              tma_load_2d(a + 8192, ta, &full[s], m_row + 64, kx + tr.a_k_off);
             }
             if (!q.b_mn) {
-              tma_load_2d(b, tb, &full[s], kb * BK, tr.n_t * q.bn);
+              tma_load_2d(b, tb, &full[s], kx + tr.b_k_off, n_row);
             } else {
-              for (int h = 0; h < q.bn / 64; ++h)
-                tma_load_2d(b + h * 8192, tb, &full[s], tr.n_t * q.bn + h * 64, kb * BK);
+              for (int h = 0; h < q.bn / 64; ++h) tma_load_2d(b + h * 8192, tb, &full[s], n_row + h * 64, kx + tr.b_k_off);
             }
           }
         }
@@ -542,8 +708,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int t = tileq[slot];
         mbar_arrive(&qempty[slot]);
         if (t < 0) break;
-        const TileRef tr = tile_of(g, t);
-        const Prob q = tr.prob ? g.p[1] : g.p[0];
+        const TileRef tr = tile_of<CG>(g, t);
+        const Prob q = g.p[tr.prob];
         const uint32_t idesc = IDESC | (static_cast<uint32_t>(q.bn >> 3) << 17) |
                                (static_cast<uint32_t>(q.a_mn) << 15) | (static_cast<uint32_t>(q.b_mn) << 16);
         const uint32_t acc = i & 1, use = i >> 1;
@@ -557,7 +723,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t a_desc0 = q.a_mn ? sdesc_sw128(smem_u32(sA), 8192, 1024) : sdesc_sw128(smem_u32(sA), 16, 1024);
         const uint64_t b_desc0 = q.b_mn ? sdesc_sw128(smem_u32(sB), 8192, 1024) : sdesc_sw128(smem_u32(sB), 16, 1024);
         const uint64_t a_kstep = q.a_mn ? 2048 >> 4 : 32 >> 4, b_kstep = q.b_mn ? 2048 >> 4 : 32 >> 4;
-        const int n_stages = (q.num_k + S::KSUB - 1) / S::KSUB;
+        const int n_stages = (tr.num_k + S::KSUB - 1) / S::KSUB;
         bool ok = true;
         for (int kb = 0; kb < n_stages; ++kb, ++it) {
           const int s = it % S::STAGES;
@@ -567,7 +733,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const int nsub = q.num_k - kb * S::KSUB < S::KSUB ? q.num_k - kb * S::KSUB : S::KSUB;
+          const int nsub = tr.num_k - kb * S::KSUB < S::KSUB ? tr.num_k - kb * S::KSUB : S::KSUB;
 #pragma unroll
           for (int j = 0; j < S::KSUB; ++j) {
             if (j < nsub) {
@@ -592,7 +758,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quad = warp & 3;  // TMEM lane quadrant this warp may access
     const int r = quad * 32 + lane;
     uint32_t seq = 0;  // staging-buffer sequence of this warp (TMA epilogues)
-    const uint32_t m_off = rank;
     // Lane 0 of each warp waits and reads the queue; the warp follows it (tcgen05.ld is
     // warp-collective, so the lanes must not part ways on a timeout).
     for (int i = 0;; ++i) {
@@ -610,7 +775,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __shfl_sync(0xffffffffu, ok, 0);
       t = __shfl_sync(0xffffffffu, t, 0);
       if (!ok || t < 0) break;
-      const TileRef tr = tile_of(g, t);
+      const TileRef tr = tile_of<CG>(g, t);
       const uint32_t acc = i & 1, use = i >> 1;
       if (lane == 0) ok = wait_or_abort(&tfull[acc], use & 1, af, ctrl);
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -618,15 +783,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * kBNMax;
-      const int m_blk = tr.m_t * CG + static_cast<int>(m_off);  // this CTA's 128-row block
-      if (tr.prob) {
-        const EpiCtx cx{&tmO1, staging};
-        e1.run(taddr, m_blk, tr.n_t, r, g.p[1].bn, cx, seq);
-      } else {
-        const EpiCtx cx{&tmO0, staging};
-        e0.run(taddr, m_blk, tr.n_t, r, g.p[0].bn, cx, seq);
-      }
+      const int m_blk = tr.m_t * CG + static_cast<int>(rank);  // this CTA's 128-row block
+      const EpiCtx cx{&maps.o[tr.prob], staging};
+      epi.run(tr, taddr, m_blk, r, g.p[tr.prob].bn, cx, seq);
       tc_fence_before();
+      if (Epi::kSignals) {
+        // The last of the four epilogue warps through this tile reports it done.  Each warp
+        // counts before it releases the accumulator, so no warp can reach the next use of
+        // the same counter (two tiles later) before all four have counted this one; nothing
+        // here waits.
+        fence_proxy_async_global();
+        __syncwarp();
+        if (lane == 0) {
+          __threadfence();
+          const uint32_t seen = atomicAdd(&epi_count[acc], 1u);
+          if (seen == kEpiWarps * use + kEpiWarps - 1) epi.done(tr);
+        }
+      }
       __syncwarp();
       if (lane == 0) {
         if (leader) mbar_arrive(&tempty[acc]);
@@ -707,14 +880,13 @@ cudaError_t kernel_units(int dev, int num_sms, int* units) {
   return cudaSuccess;
 }
 
-// Launches one or two problems.  `sched` (may be null) is the dynamic tile counter and the
+// Launches a prepared geometry.  `sched` (may be null) is the dynamic tile counter and the
 // host's record of its value, advanced by what this launch consumes (tiles + one final
 // fetch per scheduling unit), so the next launch on the stream knows its base without a
-// reset.  maps: A0, B0, A1, B1, O0, O1 (the second problem's entries repeat the first's
-// when absent).  The problems must have been made with the same `CG`.
+// reset.  The grid never exceeds the co-resident units, which the chunk backward's
+// dependency waits rely on.
 template <int CG, class Epi>
-cudaError_t launch_tc(const CUtensorMap* maps, const Prob* probs, int nprob, const Epi& e0, const Epi& e1,
-                      TileSched* sched, int num_sms, cudaStream_t st) {
+cudaError_t launch_tc(const Maps& maps, Geom g, const Epi& epi, TileSched* sched, int num_sms, cudaStream_t st) {
   using S = Shape<Epi::kStaging, CG, (CG == 2 ? Epi::kKSub : 1)>;
   static_assert(S::SMEM <= kSmemMax && S::STAGES >= 3, "shared memory budget");
   int dev = 0;
@@ -724,11 +896,6 @@ cudaError_t launch_tc(const CUtensorMap* maps, const Prob* probs, int nprob, con
   e = kernel_units<Epi, CG>(dev, num_sms, &max_units);
   if (e != cudaSuccess) return e;
   if (max_units < 1) return cudaErrorInvalidConfiguration;
-  Geom g{};
-  g.nprob = nprob;
-  g.p[0] = probs[0];
-  g.p[1] = nprob > 1 ? probs[1] : probs[0];
-  g.tiles = probs[0].tiles + (nprob > 1 ? probs[1].tiles : 0);
   if (g.tiles == 0) return cudaSuccess;
   const int units = g.tiles < max_units ? g.tiles : max_units;
   if (sched && sched->counter) {
@@ -738,7 +905,7 @@ cudaError_t launch_tc(const CUtensorMap* maps, const Prob* probs, int nprob, con
   }
   auto kern = tc_gemm_kernel<Epi, CG>;
   if (CG == 1) {
-    kern<<<units, kThreads, S::SMEM, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], g, e0, e1);
+    kern<<<units, kThreads, S::SMEM, st>>>(maps, g, epi);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
@@ -753,7 +920,17 @@ cudaError_t launch_tc(const CUtensorMap* maps, const Prob* probs, int nprob, con
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], g, e0, e1);
+  return cudaLaunchKernelEx(&cfg, kern, maps, g, epi);
+}
+
+Geom plain_geom(const Prob* probs, int nprob) {
+  Geom g{};
+  g.nprob = nprob;
+  for (int p = 0; p < nprob; ++p) {
+    g.p[p] = probs[p];
+    g.tiles += probs[p].tiles;
+  }
+  return g;
 }
 
 // Operand tensor maps.  K-major: rows of the operand are `outer`, K is `inner`.
@@ -795,56 +972,58 @@ constexpr int kLossCG = 2;
 
 }  // namespace
 
+int tc_grad_buffers() { return kGradBuffers; }
+
 cudaError_t tc_fwd_tiles(const void* Hc, const void* W, int64_t rows, int64_t d, int64_t V, float tau,
                          const int32_t* sidx, int32_t K, float* zk, float2* part, int nvt, Ctrl* ctrl,
                          TileSched* sched, int num_sms, cudaStream_t st) {
-  CUtensorMap maps[6];
-  if (!map_kmajor(&maps[0], Hc, d, rows, d, BM) || !map_kmajor(&maps[1], W, d, V, d, kTileV / kLossCG))
+  Maps maps;
+  if (!map_kmajor(&maps.a[0], Hc, d, rows, d, BM) || !map_kmajor(&maps.b[0], W, d, V, d, kTileV / kLossCG))
     return cudaErrorInvalidValue;
-  maps[2] = maps[4] = maps[0];
-  maps[3] = maps[5] = maps[1];
   FwdEpi e{rows, V, kLog2e / tau, sidx, K, zk, part, nvt, ctrl};
   const Prob p = make_prob(rows, V, d, kTileV, false, false, false, kLossCG);
-  return launch_tc<kLossCG>(maps, &p, 1, e, e, sched, num_sms, st);
+  return launch_tc<kLossCG>(maps, plain_geom(&p, 1), e, sched, num_sms, st);
 }
 
-cudaError_t tc_bwd_tiles(const void* Hc, const void* W, int64_t rows, int64_t d, int64_t V, int64_t s0, int64_t S,
-                         float tau, const int32_t* sidx, const float* sp, int32_t K, const float* lse,
-                         const uint8_t* valid, Ctrl* ctrl, void* G, int64_t ldG, TileSched* sched, int num_sms,
+cudaError_t tc_bwd_chunk(const void* Hc, const void* HcT, int64_t ldT, const void* W, int64_t rows, int64_t d,
+                         int64_t V, int64_t S, float tau, const int32_t* sidx, const float* sp, int32_t K,
+                         const float* lse, const uint8_t* valid, Ctrl* ctrl, void* G, float* dW, int dW_accumulate,
+                         float* dH_acc, unsigned int* done_g, unsigned int* done_w, TileSched* sched, int num_sms,
                          cudaStream_t st) {
-  const int64_t s_eff = (V - s0 < S) ? V - s0 : S;
-  CUtensorMap maps[6];
-  const void* Ws = static_cast<const __nv_bfloat16*>(W) + s0 * d;
-  if (!map_kmajor(&maps[0], Hc, d, rows, d, BM) || !map_kmajor(&maps[1], Ws, d, s_eff, d, kTileV / kLossCG))
-    return cudaErrorInvalidValue;
-  maps[2] = maps[4] = maps[0];
-  maps[3] = maps[5] = maps[1];
-  BwdEpi e{rows, V, s0, S, ldG, kLog2e / tau, sidx, sp, K, lse, valid, ctrl, static_cast<__nv_bfloat16*>(G)};
-  const Prob p = make_prob(rows, s_eff, d, kTileV, false, false, false, kLossCG);
-  return launch_tc<kLossCG>(maps, &p, 1, e, e, sched, num_sms, st);
-}
-
-cudaError_t tc_dW_dH(const void* G, int64_t ldG, const void* HcT, int64_t ldT, const void* W_stripe, int64_t rows,
-                     int64_t d, int64_t S, float* dW_stripe, int dW_accumulate, float* dH_acc, int dH_accumulate,
-                     Ctrl* ctrl, TileSched* sched, int num_sms, cudaStream_t st) {
-  // problem 0, dH^T[d, rows] (+)= W_s^T . G^T: A = W_s stored [S, d] (MN-major), B = G stored
-  //            [rows, S] (K-major); the epilogue writes it transposed into dH_acc[rows, d].
-  // problem 1, dW[S, d] (+)= G^T . Hc: A = G^T stored [rows, S] (MN-major), B = Hc^T stored
-  //            [d, ldT] (K-major).
-  // The dH tiles (K = S) are the longer ones and go first.  N fastest: the units in flight
-  // share their A block.
   constexpr int cg = kLossCG;
+  const int64_t ldG = kGradBuffers * S;
+  const int stripes = static_cast<int>((V + S - 1) / S);
   const int bn_h = pick_bn(rows, false), bn_w = pick_bn(d, false);
-  CUtensorMap maps[6];
-  if (!map_mnmajor(&maps[0], W_stripe, d, S, d) || !map_kmajor(&maps[1], G, S, rows, ldG, bn_h / cg) ||
-      !map_mnmajor(&maps[2], G, S, rows, ldG) || !map_kmajor(&maps[3], HcT, rows, d, ldT, bn_w / cg) ||
-      !map_out_f32(&maps[4], dH_acc, d, rows, d) || !map_out_f32(&maps[5], dW_stripe, d, S, d))
+  Maps maps;
+  // problem 0, G[rows, S] = H_chunk . W_s^T:   A = H_chunk [rows, d], B = W [V, d] (K-major)
+  // problem 1, dH^T[d, rows] += W_s^T . G^T:   A = W stored [V, d] (MN-major, K = vocab),
+  //                                            B = G buffer [rows, ldG] (K-major, K = columns)
+  // problem 2, dW[S, d] (+)= G^T . H_chunk:    A = G buffer stored [rows, ldG] (MN-major),
+  //                                            B = H_chunk^T [d, ldT] (K-major)
+  if (!map_kmajor(&maps.a[0], Hc, d, rows, d, BM) || !map_kmajor(&maps.b[0], W, d, V, d, kTileV / cg) ||
+      !map_mnmajor(&maps.a[1], W, d, V, d) || !map_kmajor(&maps.b[1], G, ldG, rows, ldG, bn_h / cg) ||
+      !map_mnmajor(&maps.a[2], G, ldG, rows, ldG) || !map_kmajor(&maps.b[2], HcT, rows, d, ldT, bn_w / cg) ||
+      !map_out_f32(&maps.o[1], dH_acc, d, rows, d) || !map_out_f32(&maps.o[2], dW, d, V, d))
     return cudaErrorInvalidValue;
-  const Prob p[2] = {make_prob(d, rows, S, bn_h, true, false, true, cg),
+  maps.o[0] = maps.o[1];
+  const Prob p[3] = {make_prob(rows, S, d, kTileV, false, false, false, cg),
+                     make_prob(d, rows, S, bn_h, true, false, true, cg),
                      make_prob(S, d, rows, bn_w, true, false, true, cg)};
-  F32Epi eh{d, rows, dH_accumulate, 1, ctrl};
-  F32Epi ew{S, d, dW_accumulate, 0, ctrl};
-  return launch_tc<cg>(maps, p, 2, eh, ew, sched, num_sms, st);
+  Geom g = plain_geom(p, 3);
+  g.stripes = stripes;
+  g.S = static_cast<int>(S);
+  g.last_cols = static_cast<int>(V - (stripes - 1) * S);
+  g.tiles = stripes * (p[0].tiles + p[1].tiles + p[2].tiles);
+  g.done_g = done_g;
+  g.done_w = done_w;
+  BwdChunkEpi e;
+  e.g = BwdEpi{rows, V, S, ldG, kLog2e / tau, sidx, sp, K, lse, valid, ctrl, static_cast<__nv_bfloat16*>(G)};
+  e.h = F32Epi{d, rows, 1, 1, 0, ctrl};
+  e.w = F32Epi{S, d, dW_accumulate, 0, S, ctrl};
+  e.ctrl = ctrl;
+  e.done_g = done_g;
+  e.done_w = done_w;
+  return launch_tc<cg>(maps, g, e, sched, num_sms, st);
 }
 
 cudaError_t tc_debug_gemm(const void* A, const void* B, float* D, int64_t M, int64_t N, int64_t K, int a_mn, int b_mn,
@@ -852,18 +1031,15 @@ cudaError_t tc_debug_gemm(const void* A, const void* B, float* D, int64_t M, int
   const int cg = cta_pair ? 2 : 1;
   if (cg == 2 && b_mn) return cudaErrorInvalidValue;
   const int bn = pick_bn(N, b_mn != 0);
-  CUtensorMap maps[6];
-  bool ok = a_mn ? map_mnmajor(&maps[0], A, M, K, M) : map_kmajor(&maps[0], A, K, M, K, BM);
-  ok = ok && (b_mn ? map_mnmajor(&maps[1], B, N, K, N) : map_kmajor(&maps[1], B, K, N, K, bn / cg));
-  ok = ok && map_out_f32(&maps[4], D, N, M, N);
+  Maps maps;
+  bool ok = a_mn ? map_mnmajor(&maps.a[0], A, M, K, M) : map_kmajor(&maps.a[0], A, K, M, K, BM);
+  ok = ok && (b_mn ? map_mnmajor(&maps.b[0], B, N, K, N) : map_kmajor(&maps.b[0], B, K, N, K, bn / cg));
+  ok = ok && map_out_f32(&maps.o[0], D, N, M, N);
   if (!ok) return cudaErrorInvalidValue;
-  maps[2] = maps[0];
-  maps[3] = maps[1];
-  maps[5] = maps[4];
-  F32Epi e{M, N, 0, 0, nullptr};
+  F32Epi e{M, N, 0, 0, 0, nullptr};
   const Prob p = make_prob(M, N, K, bn, a_mn, b_mn, true, cg);
-  if (cg == 2) return launch_tc<2>(maps, &p, 1, e, e, nullptr, num_sms, st);
-  return launch_tc<1>(maps, &p, 1, e, e, nullptr, num_sms, st);
+  if (cg == 2) return launch_tc<2>(maps, plain_geom(&p, 1), e, nullptr, num_sms, st);
+  return launch_tc<1>(maps, plain_geom(&p, 1), e, nullptr, num_sms, st);
 }
 
 }  // namespace fckl

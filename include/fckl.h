@@ -127,8 +127,10 @@ typedef enum {
   FCKL_K_FWD_TILES,    /* logit tiles + online max/sum + gather (forward) */
   FCKL_K_COMBINE,      /* per-row lse and loss_t from the tile partials */
   FCKL_K_REDUCE,       /* fixed-order mean over rows; N and the gradient scale */
-  FCKL_K_BWD_TILES,    /* recomputed logit tiles -> gradient tile G (backward) */
-  FCKL_K_GRAD_GEMM,    /* dW[stripe] (+)= G^T . H_chunk and dH_chunk (+)= G . W[stripe] */
+  FCKL_K_BWD_TILES,    /* backward: recomputed logit tiles -> gradient tile G; on the bf16
+                          path the same launch also runs dW (+)= G^T . H_chunk and
+                          dH_chunk += G . W for every vocab stripe of the chunk */
+  FCKL_K_GRAD_GEMM,    /* dW / dH contractions launched on their own (fp32 path) */
   FCKL_K_OTHER,        /* memsets and casts */
   FCKL_K_NUM_CLASSES
 } fckl_kernel_class;
