@@ -85,6 +85,7 @@ struct Prob {
   int a_mn, b_mn;  // operand layouts (see the engine)
   int n_fastest;   // raster: consecutive tiles walk N (1) or M (0)
   int bn;          // tile width: a multiple of 32 (of 64 for an MN-major B), at most 256
+  int N;           // extent of N; with a K-major B the last tile narrows to what is left
 };
 
 // A launch: up to three problems and the dynamic tile counter (a word in the workspace
@@ -113,9 +114,20 @@ constexpr int kGradBuffers = 3;
 // offsets of its operands (k: along K; m / n: along the operand's M / N rows).
 struct TileRef {
   int prob, stripe, m_t, n_t, num_k;
+  int n0, bn;  // first column of the tile (in its problem / stripe) and its width
   int a_k_off, a_m_off, b_k_off, b_n_off;
   int skip;  // entirely outside the vocabulary (chunk backward's last stripe): no work
 };
+
+// The tile's columns: [n_t * bn, +bn), except that with a K-major B operand the last tile
+// of N narrows to the columns left, rounded up to 32.  Each MMA instruction costs about
+// the same to issue whatever its width, so full-width tiles plus one narrow tile beat a
+// narrower width that divides N.
+__device__ __forceinline__ void tile_cols(const Prob& q, TileRef& r) {
+  r.n0 = r.n_t * q.bn;
+  r.bn = q.bn;
+  if (!q.b_mn && q.N - r.n0 < q.bn) r.bn = (q.N - r.n0 + 31) & ~31;
+}
 
 __device__ __forceinline__ void raster(const Prob& q, int t, int& m_t, int& n_t) {
   if (q.n_fastest) {
@@ -136,6 +148,7 @@ __device__ __forceinline__ TileRef tile_of(const Geom& g, int t) {
     r.prob = p;
     raster(g.p[p], t, r.m_t, r.n_t);
     r.num_k = g.p[p].num_k;
+    tile_cols(g.p[p], r);
     return r;
   }
   const int nG = g.p[0].tiles, nR = g.p[1].tiles + g.p[2].tiles, ns = g.stripes;
@@ -160,6 +173,7 @@ __device__ __forceinline__ TileRef tile_of(const Geom& g, int t) {
     // G[rows, S-stripe] = H_chunk . W_s^T: B rows are vocab rows s*S + n
     r.prob = 0;
     raster(g.p[0], local, r.m_t, r.n_t);
+    tile_cols(g.p[0], r);
     r.num_k = g.p[0].num_k;
     r.b_n_off = s * g.S;
     r.skip = r.n_t * g.p[0].bn >= cols;
@@ -167,6 +181,7 @@ __device__ __forceinline__ TileRef tile_of(const Geom& g, int t) {
     // dH^T[d, rows] += W_s^T . G^T: A = W rows (K) s*S.., B = G buffer columns (K) buf*S..
     r.prob = 1;
     raster(g.p[1], local, r.m_t, r.n_t);
+    tile_cols(g.p[1], r);
     r.num_k = (cols + BK - 1) / BK;
     r.a_k_off = s * g.S;
     r.b_k_off = buf * g.S;
@@ -174,6 +189,7 @@ __device__ __forceinline__ TileRef tile_of(const Geom& g, int t) {
     // dW[s*S + m, d] (+)= G^T . H_chunk: A = G buffer columns (M) buf*S..
     r.prob = 2;
     raster(g.p[2], local - g.p[1].tiles, r.m_t, r.n_t);
+    tile_cols(g.p[2], r);
     r.num_k = g.p[2].num_k;
     r.a_m_off = buf * g.S;
     r.skip = r.m_t * BM * CG >= cols;
@@ -274,12 +290,13 @@ struct FwdEpi {
   static constexpr int kKSub = 2;
   static constexpr bool kSignals = false;
 
-  __device__ __forceinline__ void run(const TileRef& tr, uint32_t taddr, int m_blk, int r, int BN, const EpiCtx&,
+  __device__ __forceinline__ void run(const TileRef& tr, uint32_t taddr, int m_blk, int r, const EpiCtx&,
                                       uint32_t&) const {
     const int64_t row = static_cast<int64_t>(m_blk) * BM + r;
     const bool live = row < rows;
     const int n_t = tr.n_t;
-    const int64_t n0 = static_cast<int64_t>(n_t) * BN;
+    const int BN = tr.bn;
+    const int64_t n0 = tr.n0;
     const int32_t* ids = sidx + (live ? row : 0) * K;
     int k = live ? lower_bound_ids(ids, K, n0) : K;
     int64_t nid = (k < K) ? ids[k] : INT64_MAX;
@@ -332,12 +349,13 @@ struct BwdEpi {
   Ctrl* ctrl;
   __nv_bfloat16* G;
 
-  __device__ __forceinline__ void run(const TileRef& tr, uint32_t taddr, int m_blk, int r, int BN,
-                                      const EpiCtx&, uint32_t&) const {
+  __device__ __forceinline__ void run(const TileRef& tr, uint32_t taddr, int m_blk, int r, const EpiCtx&,
+                                      uint32_t&) const {
     const int64_t row = static_cast<int64_t>(m_blk) * BM + r;
     const bool live = row < rows;
     const int64_t s0 = static_cast<int64_t>(tr.stripe) * S;
-    const int64_t n0l = static_cast<int64_t>(tr.n_t) * BN;
+    const int BN = tr.bn;
+    const int64_t n0l = tr.n0;
     const int64_t n0 = s0 + n0l;
     const int64_t vend = (s0 + S < V) ? s0 + S : V;
     __nv_bfloat16* Gb = G + (tr.stripe % kGradBuffers) * S;
@@ -403,11 +421,12 @@ struct F32Epi {
   static constexpr int kKSub = 2;
   static constexpr bool kSignals = false;
 
-  __device__ __forceinline__ void run(const TileRef& tr, uint32_t taddr, int m_blk, int r, int bn,
-                                      const EpiCtx& cx, uint32_t& seq) const {
+  __device__ __forceinline__ void run(const TileRef& tr, uint32_t taddr, int m_blk, int r, const EpiCtx& cx,
+                                      uint32_t& seq) const {
     const int lane = r & 31, quad = r >> 5;
     uint8_t* wbuf = cx.staging + quad * kWarpStaging;
-    const int64_t n0 = static_cast<int64_t>(tr.n_t) * bn;
+    const int bn = tr.bn;
+    const int64_t n0 = tr.n0;
     const int64_t m0 = static_cast<int64_t>(m_blk) * BM + quad * 32;
     const int64_t y0 = static_cast<int64_t>(tr.stripe) * y_stripe;
 #pragma unroll 1
@@ -468,14 +487,14 @@ struct BwdChunkEpi {
   unsigned int* done_w;
 
   static constexpr int kStaging = F32Epi::kStaging;
-  static constexpr int kKSub = 1;
+  static constexpr int kKSub = 2;
   static constexpr bool kSignals = true;
 
-  __device__ __forceinline__ void run(const TileRef& tr, uint32_t taddr, int m_blk, int r, int bn,
-                                      const EpiCtx& cx, uint32_t& seq) const {
-    if (tr.prob == 0) g.run(tr, taddr, m_blk, r, bn, cx, seq);
-    else if (tr.prob == 1) h.run(tr, taddr, m_blk, r, bn, cx, seq);
-    else w.run(tr, taddr, m_blk, r, bn, cx, seq);
+  __device__ __forceinline__ void run(const TileRef& tr, uint32_t taddr, int m_blk, int r, const EpiCtx& cx,
+                                      uint32_t& seq) const {
+    if (tr.prob == 0) g.run(tr, taddr, m_blk, r, cx, seq);
+    else if (tr.prob == 1) h.run(tr, taddr, m_blk, r, cx, seq);
+    else w.run(tr, taddr, m_blk, r, cx, seq);
   }
 
   __device__ __forceinline__ void done(const TileRef& tr) const {
@@ -647,8 +666,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // bytes of one sub-block, both CTAs' boxes
         const uint32_t tx_sub = static_cast<uint32_t>(CG * S::A_SUB + q.bn * BK * 2);
         const int m_row = (tr.m_t * CG + static_cast<int>(rank)) * BM + tr.a_m_off;
-        const int b_rows = q.bn / CG;
-        const int n_row = tr.n_t * q.bn + static_cast<int>(rank) * b_rows + tr.b_n_off;
+        // a CTA pair splits the tile's columns in halves (a narrow last tile too); the box
+        // is the problem's full half-width either way, its excess rows unused
+        const int n_row = tr.n0 + static_cast<int>(rank) * (tr.bn / CG) + tr.b_n_off;
         const int n_stages = (tr.num_k + S::KSUB - 1) / S::KSUB;
         bool ok = true;
         for (int kb = 0; kb < n_stages; ++kb, ++it) {
@@ -710,7 +730,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (t < 0) break;
         const TileRef tr = tile_of<CG>(g, t);
         const Prob q = g.p[tr.prob];
-        const uint32_t idesc = IDESC | (static_cast<uint32_t>(q.bn >> 3) << 17) |
+        const uint32_t idesc = IDESC | (static_cast<uint32_t>(tr.bn >> 3) << 17) |
                                (static_cast<uint32_t>(q.a_mn) << 15) | (static_cast<uint32_t>(q.b_mn) << 16);
         const uint32_t acc = i & 1, use = i >> 1;
         if (!wait_or_abort(&tempty[acc], (use & 1) ^ 1, af, ctrl)) break;
@@ -785,7 +805,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * kBNMax;
       const int m_blk = tr.m_t * CG + static_cast<int>(rank);  // this CTA's 128-row block
       const EpiCtx cx{&maps.o[tr.prob], staging};
-      epi.run(tr, taddr, m_blk, r, g.p[tr.prob].bn, cx, seq);
+      epi.run(tr, taddr, m_blk, r, cx, seq);
       tc_fence_before();
       if (Epi::kSignals) {
         // The last of the four epilogue warps through this tile reports it done.  Each warp
@@ -838,6 +858,7 @@ Prob make_prob(int64_t M, int64_t N, int64_t K, int bn, bool a_mn, bool b_mn, bo
   q.b_mn = b_mn;
   q.n_fastest = n_fastest;
   q.bn = bn;
+  q.N = static_cast<int>(N);
   return q;
 }
 
@@ -945,22 +966,22 @@ bool map_out_f32(CUtensorMap* m, const float* base, int64_t cols, int64_t rows, 
   return encode_tmap_f32_2d(m, base, cols, rows, ld * 4, 32, 32);
 }
 
-// Tile width over N: the candidate with the least padded work, counting a fixed cost of 32
-// columns per tile for its ramp-up and epilogue.  An MN-major B needs a multiple of 64;
-// otherwise multiples of 32 are allowed (the epilogues work in 32-column chunks; a CTA
-// pair's half of B is then a multiple of 16 rows, whole 8-row swizzle atoms).
+// Tile width over N.  With a K-major B: 256 (the widest MMA), the last tile narrowing to
+// what is left (a multiple of 32: the epilogues work in 32-column chunks, and a CTA pair's
+// half of B is then a multiple of 16 rows, whole 8-row swizzle atoms); N below 256 gets
+// one tile of N rounded up to 32.  An MN-major B loads 64-column boxes and does not
+// narrow: the candidate multiple of 64 with the least padded work, counting a fixed cost
+// of 32 columns per tile.
 int pick_bn(int64_t N, bool b_mn) {
+  if (!b_mn) return N >= 256 ? 256 : static_cast<int>((N + 31) / 32 * 32);
   static const int mn[] = {256, 192, 128, 64};
-  static const int km[] = {256, 224, 192, 160, 128, 96, 64, 32};
-  const int* c = b_mn ? mn : km;
-  const int n = b_mn ? 4 : 8;
-  int best = c[0];
+  int best = mn[0];
   int64_t best_cost = INT64_MAX;
-  for (int i = 0; i < n; ++i) {
-    const int64_t cost = (N + c[i] - 1) / c[i] * (c[i] + 32);
+  for (int c : mn) {
+    const int64_t cost = (N + c - 1) / c * (c + 32);
     if (cost < best_cost) {
       best_cost = cost;
-      best = c[i];
+      best = c;
     }
   }
   return best;
