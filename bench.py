@@ -45,8 +45,27 @@ def algorithmic_flops(T, d, V, n_valid):
 
 
 def dist_env():
+    """(rank, local_rank, world_size) from the launcher's environment (1 process: 0, 0, 1)."""
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     return int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")), ws
+
+
+def max_over_ranks(x, dist=None, device="cpu"):
+    """The largest of every rank's x: a job's time is that of its slowest rank.  `dist` is
+    torch.distributed with an initialized group (None: one process)."""
+    if dist is None:
+        return float(x)
+    import torch
+
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank, world, seconds):
+    """Whole-job throughput when every rank processes its own batch of `units_per_rank`
+    (token-sharded replicas, weak scaling)."""
+    return world * units_per_rank / seconds
 
 
 class ClockSampler:
@@ -196,6 +215,66 @@ def run_memory_curve(args, cfg):
                           points=points)), flush=True)
 
 
+def run_topk(args, cfg):
+    """Teacher top-K extraction (the offline step that builds the cache): the K largest
+    logits and their ids per row of a [T, V] bf16 teacher logit matrix of the workload's
+    vocabulary (offset - 1.1 ln(v+1) + Gumbel noise, whose per-row top-K ids are Zipf(1.1)
+    draws without replacement).  HBM-bound: the roofline is the measured copy bandwidth."""
+    import torch
+
+    from chunked_kl_loss_head_b300 import api
+    from gen import bf16_bits_to_f32, make_teacher_logits
+
+    if args.warmup < 3:
+        args.warmup = 3
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    peaks = load_peaks()
+    T = args.topk_rows
+    V, K = cfg.V, cfg.K
+    host = make_teacher_logits(T, V, seed=cfg.seed, dtype="bf16")
+    x = torch.from_numpy(host.view(np.int16)).view(torch.bfloat16).to(dev)
+    idx = torch.empty((T, K), dtype=torch.int32, device=dev)
+    val = torch.empty((T, K), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        api.fckl_topk_extract(x, K, idx, val, stream)
+    torch.cuda.synchronize(dev)
+    launches0 = api.fckl_launch_count()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler("0") as clk:
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(args.steps):
+            api.fckl_topk_extract(x, K, idx, val, stream)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / args.steps
+    launches = api.fckl_launch_count() - launches0
+    algo_bytes = T * V * 2 + T * K * 8
+    gbs = algo_bytes / (ms / 1e3) / 1e9
+    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    cpu = None
+    if not args.no_cpu:
+        from oracle import topk_rows
+
+        rows = 8
+        t0 = time.perf_counter()
+        topk_rows(bf16_bits_to_f32(host[:rows]), K)
+        secs = time.perf_counter() - t0
+        cpu = dict(value=rows / secs, unit="rows/s", cores=len(os.sched_getaffinity(0)), kind="oracle",
+                   sample=f"oracle top-K (numpy lexsort per row) on rows 0..{rows - 1}; {secs:.2f} s")
+    line = dict(metric="teacher top-K extraction rows/s", value=T / (ms / 1e3), unit="rows/s", n_gpus=1,
+                steps=args.steps, warmup=args.warmup, ms_per_step=ms, higher_is_better=True, scaling="weak",
+                vs_baseline=None, dtype="bf16", data="synthetic",
+                config=dict(workload=f"teacher logits [T={T}, V={V}] bf16, K={K}",
+                            l2=f"input larger than L2 ({T * V * 2 / 1e9:.2f} GB)"),
+                roofline=dict(bound="hbm", achieved=gbs, peak=hbm, unit="GB/s", frac=gbs / hbm, traffic=None,
+                              peak_note=f"HBM copy ({peaks['source']})"),
+                cpu_baseline=cpu, gpu_launches=int(launches), clocks=clk.summary())
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -209,6 +288,9 @@ def main():
     ap.add_argument("--shape", default="", help="override T,d,V,K of the workload (e.g. a small ncu case)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--topk-rows", type=int, default=4096, help="rows of the --path topk workload")
+    ap.add_argument("--path", default="loss", choices=["loss", "topk"],
+                    help="topk: time the teacher top-K extraction instead (one JSON line)")
     ap.add_argument("--memory-curve", default="",
                     help="comma-separated token counts: peak device memory of one fwd+bwd of the workload's "
                          "shape at each T (one JSON line), instead of the timing run")
@@ -226,6 +308,9 @@ def main():
         return
     if args.memory_curve:
         run_memory_curve(args, cfg)
+        return
+    if args.path == "topk":
+        run_topk(args, cfg)
         return
     if args.warmup < 3:
         args.warmup = 3  # timing rule: at least three warm-up steps
@@ -310,17 +395,13 @@ def main():
     status = api.fckl_get_error(ws)
     if status != 0:
         raise SystemExit(f"device status after the timed region: {api.fckl_status_string(status)}")
-    t_max = ms
-    if dist is not None:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_max = float(tt.item())
+    t_max = max_over_ranks(ms, dist, dev)
     peak_alloc = torch.cuda.max_memory_allocated(dev)
     free1, _ = torch.cuda.mem_get_info(dev)
     loss_val = float(loss.item())
 
     sec_per_step = t_max / 1e3 / args.steps
-    tokens_per_s = world * T / sec_per_step
+    tokens_per_s = job_rate(T, world, sec_per_step)
     flops = algorithmic_flops(T, d, V, n_valid)
     tflops = flops / sec_per_step / 1e12
 
@@ -376,12 +457,8 @@ def main():
             loss_host.copy_(loss, non_blocking=True)
             stream.synchronize()
         barrier()
-        e2e_s = (time.perf_counter() - t0) / n_e2e
-        if dist is not None:
-            tt = torch.tensor([e2e_s], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            e2e_s = float(tt.item())
-        e2e = dict(value=world * T / e2e_s, unit="tokens/s", h2d_bytes_per_step=int(h2d), d2h_bytes_per_step=4,
+        e2e_s = max_over_ranks((time.perf_counter() - t0) / n_e2e, dist, dev)
+        e2e = dict(value=job_rate(T, world, e2e_s), unit="tokens/s", h2d_bytes_per_step=int(h2d), d2h_bytes_per_step=4,
                    ms_per_step=1e3 * e2e_s, steps=n_e2e)
         del dst, pinned
 

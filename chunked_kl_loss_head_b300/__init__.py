@@ -20,8 +20,10 @@ from .api import (  # noqa: F401
     fckl_profile_enable,
     fckl_profile_read,
     fckl_status_string,
+    fckl_topk_extract,
     fckl_workspace_size,
     forward,
+    topk_extract,
     workspace,
 )
 from .autograd import FusedChunkedKLLoss, fused_chunked_kl_loss  # noqa: F401

@@ -17,7 +17,7 @@ from ._lib import lib
 F32, BF16 = 0, 1
 STATUS = {0: "FCKL_OK", 1: "FCKL_ERR_INVALID_ARG", 2: "FCKL_ERR_UNSUPPORTED", 3: "FCKL_ERR_WORKSPACE",
           4: "FCKL_ERR_CUDA", 5: "FCKL_ERR_BAD_INDEX", 6: "FCKL_ERR_TIMEOUT"}
-KERNEL_CLASSES = ["prep", "fwd_tiles", "combine", "reduce", "bwd_tiles", "grad_gemm", "other"]
+KERNEL_CLASSES = ["prep", "fwd_tiles", "combine", "reduce", "bwd_tiles", "grad_gemm", "other", "topk"]
 
 
 class FcklError(RuntimeError):
@@ -107,6 +107,29 @@ def fckl_forward_noalloc(H, W, topk_idx, topk_logits, valid, tau, chunk, loss, l
                                     float(tau), int(chunk), _dtype_code(H), _ptr(loss), _ptr(lse), _ptr(row_loss),
                                     _ptr(status), _stream(stream))
     _check(st, "fckl_forward_noalloc")
+
+
+def fckl_topk_extract(logits, K, topk_idx, topk_logits, stream=None):
+    """Per row of logits [T, V] (float32 or bfloat16): the K largest values and their ids,
+    value descending then id ascending, into topk_idx [T, K] int32 / topk_logits float32."""
+    if logits.dim() != 2:
+        raise ValueError("logits must be [T, V]")
+    T, V = logits.shape
+    if topk_idx.shape != (T, K) or topk_logits.shape != (T, K):
+        raise ValueError("outputs must be [T, K]")
+    if topk_idx.dtype != torch.int32 or topk_logits.dtype != torch.float32:
+        raise TypeError("topk_idx int32 and topk_logits float32 expected")
+    _check(lib().fckl_topk_extract(_ptr(logits), T, V, int(K), _dtype_code(logits), _ptr(topk_idx),
+                                   _ptr(topk_logits), _stream(stream)), "fckl_topk_extract")
+
+
+def topk_extract(logits, K, stream=None):
+    """(topk_idx [T, K] int32, topk_logits [T, K] float32) on logits' device."""
+    T = logits.shape[0]
+    idx = torch.empty((T, K), dtype=torch.int32, device=logits.device)
+    val = torch.empty((T, K), dtype=torch.float32, device=logits.device)
+    fckl_topk_extract(logits, K, idx, val, stream)
+    return idx, val
 
 
 def fckl_get_error(ws, stream=None) -> int:

@@ -363,6 +363,20 @@ fckl_status fckl_backward(const void* H, const void* W, const int32_t* topk_idx,
   return FCKL_OK;
 }
 
+fckl_status fckl_topk_extract(const void* logits, int64_t T, int64_t V, int32_t K, fckl_dtype dtype,
+                              int32_t* topk_idx, float* topk_logits, void* stream) {
+  if (T < 0 || V < 1 || V >= (int64_t(1) << 31) || T >= (int64_t(1) << 31)) return FCKL_ERR_INVALID_ARG;
+  if (K < 1 || K > FCKL_MAX_K || K > V) return FCKL_ERR_INVALID_ARG;
+  if (dtype != FCKL_F32 && dtype != FCKL_BF16) return FCKL_ERR_INVALID_ARG;
+  if (T > 0 && (!logits || !topk_idx || !topk_logits)) return FCKL_ERR_INVALID_ARG;
+  if (!aligned(logits, dtype == FCKL_BF16 ? 2 : 4) || !aligned(topk_idx, 4) || !aligned(topk_logits, 4))
+    return FCKL_ERR_UNSUPPORTED;
+  int num_sms = 0;
+  FCKL_TRY(device_info(&num_sms));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return step(FCKL_K_TOPK, st, [&] { return launch_topk(logits, T, V, K, dtype, topk_idx, topk_logits, st); });
+}
+
 fckl_status fckl_get_error(void* ws, void* stream) {
   if (!ws) return FCKL_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

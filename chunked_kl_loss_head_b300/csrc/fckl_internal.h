@@ -67,6 +67,10 @@ cudaError_t launch_f32_to_bf16(const float* src, void* dst, int64_t n, cudaStrea
 cudaError_t launch_transpose_bf16(const void* in, int64_t rows, int64_t cols, int64_t ld_in, void* out,
                                   int64_t ld_out, cudaStream_t st);
 
+// ---- teacher top-K extraction (fckl_topk.cu) ----------------------------------------------
+cudaError_t launch_topk(const void* logits, int64_t T, int64_t V, int32_t K, fckl_dtype dtype,
+                        int32_t* idx, float* val, cudaStream_t st);
+
 // ---- fp32 CUDA-core path (fckl_simt.cu) --------------------------------------------------
 cudaError_t launch_simt_fwd_tiles(const float* Hc, const float* W, int64_t rows, int64_t d, int64_t V,
                                   float tau, const int32_t* sidx, int32_t K, float* zk, float2* part,

@@ -1,0 +1,276 @@
+// fckl_topk.cu -- teacher top-K extraction: per row of a [T, V] logit matrix, the K largest
+// logits and their ids, the preparation step of the offline cache the loss consumes
+// (getaibook.com, "Preparing Offline Top-K Logits").
+//
+// Order: value descending, then id ascending, values compared through order-preserving
+// unsigned keys of their float32 bit patterns (sign-magnitude flipped), so every row has
+// one exact answer even with ties.
+//
+// One CTA per row, HBM-bound: the row is streamed once.  A strided sample of the row
+// (2048 keys) is sorted in shared memory and its r-th largest key, r chosen so that a few
+// times K row entries are expected above it, becomes a filter threshold; the streaming
+// pass appends every entry at or above it to a shared-memory candidate list (warp-aggregated
+// appends, one shared atomic per warp and 8-entry vector), and a bitonic sort of the
+// candidates by (key, id) gives the answer.  When the sample misleads (fewer than K
+// candidates, or more than the list holds: heavy ties, tiny or adversarial rows) the row
+// takes the exact path: a 4-pass radix select of the K-th largest key, then every entry
+// above it plus the entries equal to it in id order.
+#include <cuda_bf16.h>
+
+#include <cstdint>
+
+#include "fckl_internal.h"
+
+namespace fckl {
+namespace {
+
+constexpr int kTkThreads = 512;
+constexpr int kTkWarps = kTkThreads / 32;
+constexpr int kSample = 2048;  // sampled keys per row, 4 per thread
+constexpr int kCap = 8192;     // candidates a row may keep
+constexpr unsigned kFull = 0xffffffffu;
+
+struct TkSmem {
+  unsigned long long cand[kCap];  // (key << 32) | (0xffffffff - id): larger = earlier in the order
+  uint32_t sample[kSample];
+  uint32_t hist[256];
+  uint32_t warp_sum[kTkWarps];
+  uint32_t count;
+  uint32_t thr;
+  uint32_t need;
+  uint32_t taken;
+};
+
+__device__ __forceinline__ uint32_t key_of_bits(uint32_t u) { return (u & 0x80000000u) ? ~u : (u | 0x80000000u); }
+__device__ __forceinline__ uint32_t bits_of_key(uint32_t k) { return (k & 0x80000000u) ? (k & 0x7fffffffu) : ~k; }
+
+template <class E>
+__device__ __forceinline__ uint32_t bits_at(const E* row, int64_t i);
+template <>
+__device__ __forceinline__ uint32_t bits_at<uint16_t>(const uint16_t* row, int64_t i) {
+  return static_cast<uint32_t>(row[i]) << 16;
+}
+template <>
+__device__ __forceinline__ uint32_t bits_at<uint32_t>(const uint32_t* row, int64_t i) {
+  return row[i];
+}
+
+__device__ __forceinline__ unsigned long long composite(uint32_t key, int64_t id) {
+  return (static_cast<unsigned long long>(key) << 32) | (0xffffffffull - static_cast<unsigned long long>(id));
+}
+
+// Bitonic sort of n (a power of two) values in shared memory, descending.
+template <class U>
+__device__ void bitonic_desc(U* s, int n) {
+  for (int k = 2; k <= n; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < n; i += kTkThreads) {
+        const int ixj = i ^ j;
+        if (ixj > i) {
+          const U a = s[i], b = s[ixj];
+          const bool desc_block = (i & k) == 0;
+          if (desc_block ? (a < b) : (a > b)) {
+            s[i] = b;
+            s[ixj] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+// Appends (key, id) when `pred`: one shared atomic per warp.  Every lane of the warp must
+// call it (the ballot is warp-wide).
+__device__ __forceinline__ void append(TkSmem& sm, bool pred, uint32_t key, int64_t id) {
+  const unsigned mask = __ballot_sync(kFull, pred);
+  if (!mask) return;
+  const int lane = threadIdx.x & 31;
+  const int leader = __ffs(mask) - 1;
+  uint32_t base = 0;
+  if (lane == leader) base = atomicAdd(&sm.count, static_cast<uint32_t>(__popc(mask)));
+  base = __shfl_sync(kFull, base, leader);
+  if (pred) {
+    const uint32_t pos = base + static_cast<uint32_t>(__popc(mask & ((1u << lane) - 1u)));
+    if (pos < static_cast<uint32_t>(kCap)) sm.cand[pos] = composite(key, id);
+  }
+}
+
+// Calls f(key, id, valid) for every entry of the row, the lanes of each warp together (a
+// fixed number of iterations per warp, valid = false past the end), vectorized when the
+// row is 16-byte aligned.
+template <class E, class F>
+__device__ __forceinline__ void for_each_key(const E* row, int64_t V, F&& f) {
+  constexpr int kVec = 16 / sizeof(E);
+  const uintptr_t addr = reinterpret_cast<uintptr_t>(row);
+  if (addr % 16 == 0) {
+    const int64_t nvec = V / kVec;
+    const uint4* rv = reinterpret_cast<const uint4*>(row);
+    const int64_t iters = (nvec + kTkThreads - 1) / kTkThreads;
+    for (int64_t it = 0; it < iters; ++it) {
+      const int64_t v = it * kTkThreads + threadIdx.x;
+      uint4 q = make_uint4(0, 0, 0, 0);
+      const bool ok = v < nvec;
+      if (ok) q = __ldcs(rv + v);
+      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int e = 0; e < kVec; ++e) {
+        uint32_t u;
+        if (sizeof(E) == 2) u = (e & 1) ? (w[e >> 1] & 0xffff0000u) : (w[e >> 1] << 16);
+        else u = w[e];
+        f(key_of_bits(u), v * kVec + e, ok);
+      }
+    }
+    const int64_t tail0 = nvec * kVec;
+    if (tail0 < V) {  // fewer than kVec entries: one warp-wide round
+      const int64_t i = tail0 + threadIdx.x;
+      const bool ok = i < V;
+      f(ok ? key_of_bits(bits_at(row, i)) : 0u, i, ok);
+    }
+  } else {
+    const int64_t iters = (V + kTkThreads - 1) / kTkThreads;
+    for (int64_t it = 0; it < iters; ++it) {
+      const int64_t i = it * kTkThreads + threadIdx.x;
+      const bool ok = i < V;
+      f(ok ? key_of_bits(bits_at(row, i)) : 0u, i, ok);
+    }
+  }
+}
+
+// Exclusive prefix of `flag` over the CTA in thread order: returns this thread's rank and
+// the CTA total through `total` (the same for every thread).
+__device__ __forceinline__ uint32_t cta_rank(TkSmem& sm, bool flag, uint32_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const unsigned m = __ballot_sync(kFull, flag);
+  if (lane == 0) sm.warp_sum[warp] = static_cast<uint32_t>(__popc(m));
+  __syncthreads();
+  uint32_t before = 0, all = 0;
+  for (int w = 0; w < kTkWarps; ++w) {
+    const uint32_t c = sm.warp_sum[w];
+    before += w < warp ? c : 0;
+    all += c;
+  }
+  __syncthreads();
+  *total = all;
+  return before + static_cast<uint32_t>(__popc(m & ((1u << lane) - 1u)));
+}
+
+template <class E>
+__global__ void __launch_bounds__(kTkThreads) topk_kernel(const E* __restrict__ logits, int64_t V, int K,
+                                                          int32_t* __restrict__ out_idx,
+                                                          float* __restrict__ out_val) {
+  extern __shared__ __align__(16) uint8_t tk_raw[];
+  TkSmem& sm = *reinterpret_cast<TkSmem*>(tk_raw);
+  const int64_t t = blockIdx.x;
+  const E* row = logits + t * V;
+  const int tid = threadIdx.x;
+
+  // ---- fast path: threshold from a sample, one streaming pass, sort the candidates
+  uint32_t thr = 0;  // V <= kCap: keep every entry
+  if (V > kCap) {
+    const int64_t stride = V / (kSample / 4);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) sm.sample[tid * 4 + e] = key_of_bits(bits_at(row, tid * stride + e));
+    __syncthreads();
+    bitonic_desc(sm.sample, kSample);
+    // about 1.5 K + 16 samples' worth of row entries expected at or above the threshold
+    int r = static_cast<int>((3ll * K * kSample + 2 * V - 1) / (2 * V)) + 16;
+    if (r > kSample - 1) r = kSample - 1;
+    thr = sm.sample[r];
+  }
+  if (tid == 0) sm.count = 0;
+  __syncthreads();
+  for_each_key(row, V, [&](uint32_t key, int64_t id, bool ok) { append(sm, ok && key >= thr, key, id); });
+  __syncthreads();
+  uint32_t n = sm.count;
+  bool exact = n < static_cast<uint32_t>(K) || n > static_cast<uint32_t>(kCap);
+
+  if (exact) {
+    // ---- exact path: radix select of the K-th largest key, 8 bits per pass
+    uint32_t prefix = 0, pmask = 0;
+    uint32_t need = static_cast<uint32_t>(K);
+    for (int shift = 24; shift >= 0; shift -= 8) {
+      for (int b = tid; b < 256; b += kTkThreads) sm.hist[b] = 0;
+      __syncthreads();
+      for_each_key(row, V, [&](uint32_t key, int64_t, bool ok) {
+        if (ok && (key & pmask) == prefix) atomicAdd(&sm.hist[(key >> shift) & 255u], 1u);
+      });
+      __syncthreads();
+      if (tid == 0) {
+        uint32_t cum = 0;
+        int bin = 0;
+        for (int b = 255; b >= 0; --b) {
+          if (cum + sm.hist[b] >= need) {
+            bin = b;
+            break;
+          }
+          cum += sm.hist[b];
+        }
+        sm.need = need - cum;
+        sm.thr = prefix | (static_cast<uint32_t>(bin) << shift);
+      }
+      __syncthreads();
+      need = sm.need;
+      prefix = sm.thr;
+      pmask |= 255u << shift;
+    }
+    // every entry above the K-th largest key (fewer than K), then `need` entries equal to
+    // it, the smallest ids first (the row is walked in id order, one CTA-wide round at a time)
+    const uint32_t kth = prefix;
+    if (tid == 0) sm.count = 0;
+    __syncthreads();
+    for_each_key(row, V, [&](uint32_t key, int64_t id, bool ok) { append(sm, ok && key > kth, key, id); });
+    __syncthreads();
+    const uint32_t above = sm.count;
+    uint32_t taken = 0;
+    const int64_t rounds = (V + kTkThreads - 1) / kTkThreads;
+    for (int64_t it = 0; it < rounds && taken < need; ++it) {
+      const int64_t i = it * kTkThreads + tid;
+      const bool eq = i < V && key_of_bits(bits_at(row, i)) == kth;
+      uint32_t total;
+      const uint32_t rank = cta_rank(sm, eq, &total);
+      if (eq && taken + rank < need) sm.cand[above + taken + rank] = composite(kth, i);
+      taken += total;
+    }
+    n = static_cast<uint32_t>(K);
+    __syncthreads();
+  }
+
+  // ---- sort the candidates (padded with zeros, which sort last) and write the first K
+  int np2 = 1;
+  while (np2 < static_cast<int>(n)) np2 <<= 1;
+  for (int i = static_cast<int>(n) + tid; i < np2; i += kTkThreads) sm.cand[i] = 0ull;
+  __syncthreads();
+  bitonic_desc(sm.cand, np2);
+  for (int k = tid; k < K; k += kTkThreads) {
+    const unsigned long long c = sm.cand[k];
+    const uint32_t key = static_cast<uint32_t>(c >> 32);
+    out_idx[t * K + k] = static_cast<int32_t>(0xffffffffu - static_cast<uint32_t>(c & 0xffffffffull));
+    out_val[t * K + k] = __uint_as_float(bits_of_key(key));
+  }
+}
+
+}  // namespace
+
+size_t topk_smem_bytes() { return sizeof(TkSmem); }
+
+cudaError_t launch_topk(const void* logits, int64_t T, int64_t V, int32_t K, fckl_dtype dtype, int32_t* idx,
+                        float* val, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  const size_t smem = sizeof(TkSmem);
+  cudaError_t e;
+  if (dtype == FCKL_BF16) {
+    e = cudaFuncSetAttribute(topk_kernel<uint16_t>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    topk_kernel<uint16_t><<<static_cast<unsigned>(T), kTkThreads, smem, st>>>(static_cast<const uint16_t*>(logits), V,
+                                                                              K, idx, val);
+  } else {
+    e = cudaFuncSetAttribute(topk_kernel<uint32_t>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    topk_kernel<uint32_t><<<static_cast<unsigned>(T), kTkThreads, smem, st>>>(static_cast<const uint32_t*>(logits), V,
+                                                                              K, idx, val);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace fckl

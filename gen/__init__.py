@@ -9,6 +9,7 @@ from .synthetic import (  # noqa: F401
     make_inputs,
     make_rows,
     make_small,
+    make_teacher_logits,
     make_W,
     valid_mask,
 )

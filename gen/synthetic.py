@@ -41,7 +41,7 @@ import numpy as np
 
 ROWS_PER_BLOCK = 1024
 
-_TAG_H, _TAG_W, _TAG_IDS, _TAG_GUMBEL, _TAG_MASK, _TAG_ONEHOT, _TAG_FALLBACK = range(1, 8)
+_TAG_H, _TAG_W, _TAG_IDS, _TAG_GUMBEL, _TAG_MASK, _TAG_ONEHOT, _TAG_FALLBACK, _TAG_TEACHER = range(1, 9)
 
 
 @dataclasses.dataclass(frozen=True)
@@ -343,3 +343,36 @@ def make_small(T, d, V, K, tau=1.0, dtype="bf16", seed=0, ids="zipf", mask="none
                  mask=mask, mask_frac=mask_frac, onehot_frac=onehot_frac,
                  logit_offset=logit_offset, seed=seed)
     return make_inputs(cfg)
+
+
+# ----------------------------------------------------------------------------------------
+# full teacher logits (the input of the top-K extraction that builds the cache)
+
+
+_TEACHER_ROWS = 64  # rows per random stream of the teacher logits (V-wide rows are large)
+
+
+def _teacher_block(seed, b, n_total, V, zipf_a, offset, dtype):
+    n = min(_TEACHER_ROWS, n_total - b * _TEACHER_ROWS)
+    bias = (offset - zipf_a * np.log1p(np.arange(V, dtype=np.float64))).astype(np.float32)
+    # Gumbel(0, 1) = -ln(-ln u), u uniform on (0, 1), in float32 (u kept off 0 and 1)
+    u = _rng(seed, _TAG_TEACHER, b).random((n, V), dtype=np.float32)
+    u *= np.float32(1.0 - 2.0 ** -23)
+    u += np.float32(2.0 ** -24)
+    np.log(u, out=u)
+    np.negative(u, out=u)
+    np.log(u, out=u)
+    x = bias - u
+    return f32_to_bf16_bits(x) if dtype == "bf16" else x
+
+
+def make_teacher_logits(T, V, seed=0, dtype="bf16", zipf_a=1.1, offset=12.0):
+    """Full teacher logits [T, V]: offset - zipf_a * ln(v + 1) + Gumbel(0, 1) per entry
+    (bf16 bit patterns or float32).  With this bias the K largest entries of a row are a
+    sample of K distinct ids from Zipf(zipf_a) drawn without replacement (the Gumbel top-k
+    property), the distribution of the cached ids of the loss workloads."""
+    nb = (T + _TEACHER_ROWS - 1) // _TEACHER_ROWS
+    parts = _pool_map(lambda b: _teacher_block(seed, b, T, V, zipf_a, offset, dtype), range(nb))
+    if not parts:
+        return np.zeros((0, V), np.uint16 if dtype == "bf16" else np.float32)
+    return np.concatenate(parts, axis=0)

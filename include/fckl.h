@@ -112,6 +112,24 @@ FCKL_API fckl_status fckl_backward(const void* H, const void* W, const int32_t* 
                           const float* lse, float grad_loss, const float* grad_scale, void* dH,
                           float* dW, void* ws, size_t ws_bytes, void* stream);
 
+/* Teacher top-K extraction, the offline step that builds the cache the loss reads: the
+ * teacher is run once and only its K largest logits per token position are kept, with
+ * their ids (getaibook.com, "Preparing Offline Top-K Logits"; axbrief.com, "Breaking the
+ * Bottleneck with Offline Caching and Chunked Loss").  For every row t of logits[T, V]
+ * (`dtype` elements, row-major, contiguous) writes the K entries that come first in the
+ * order value descending, then id ascending:
+ *   topk_idx    device int32 [T, K]: their ids, in that order
+ *   topk_logits device float32 [T, K]: their values widened to float32 (exact)
+ * so the output is unique even where values tie, and is the topk_idx / topk_logits input
+ * of fckl_forward as is.  Values are ordered by their bit patterns read as sign-magnitude
+ * numbers: numeric order for all non-NaN values, -0 just below +0, NaNs with the sign bit
+ * clear above +inf and with it set below -inf.  Needs 1 <= K <= min(V, FCKL_MAX_K) and
+ * V < 2^31 (FCKL_ERR_INVALID_ARG), logits aligned to its element size and the outputs to
+ * 4 bytes (FCKL_ERR_UNSUPPORTED).  Allocates nothing and keeps no state; asynchronous on
+ * `stream`; returns FCKL_OK once the work is queued. */
+FCKL_API fckl_status fckl_topk_extract(const void* logits, int64_t T, int64_t V, int32_t K, fckl_dtype dtype,
+                                       int32_t* topk_idx, float* topk_logits, void* stream);
+
 /* Waits for `stream`, then returns and clears the status word the GPU wrote in
  * the workspace (FCKL_OK, FCKL_ERR_BAD_INDEX or FCKL_ERR_TIMEOUT), or
  * FCKL_ERR_CUDA when the wait or the copy itself failed. */
@@ -132,6 +150,7 @@ typedef enum {
                           dH_chunk += G . W for every vocab stripe of the chunk */
   FCKL_K_GRAD_GEMM,    /* dW / dH contractions launched on their own (fp32 path) */
   FCKL_K_OTHER,        /* memsets and casts */
+  FCKL_K_TOPK,         /* teacher top-K extraction (fckl_topk_extract) */
   FCKL_K_NUM_CLASSES
 } fckl_kernel_class;
 

@@ -93,3 +93,14 @@ def test_valid_arguments_need_a_device():
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     assert _fwd() in (2, 4)
+
+
+def test_topk_rejects_bad_arguments():
+    L = _lib.lib()
+    p = ctypes.c_void_p(1 << 20)
+    # K > V, K < 1, K above the limit, a bad dtype, T < 0: refused before any device work
+    for T, V, K, dt in ((4, 100, 101, BF16), (4, 100, 0, BF16), (4, 5000, 1025, F32), (4, 100, 10, 7),
+                        (-1, 100, 10, BF16)):
+        assert L.fckl_topk_extract(p, T, V, K, dt, p, p, None) == 1
+    # misaligned logits for fp32
+    assert L.fckl_topk_extract(ctypes.c_void_p((1 << 20) + 2), 4, 100, 10, F32, p, p, None) == 2
