@@ -7,8 +7,8 @@
 // one exact answer even with ties.
 //
 // One CTA per row, HBM-bound: the row is streamed once.  A strided sample of the row
-// (2048 keys) is sorted in shared memory and its r-th largest key, r chosen so that a few
-// times K row entries are expected above it, becomes a filter threshold; the streaming
+// (2048 keys) is radix-selected for a key with r sampled keys above it, r chosen so that
+// a few times K row entries are expected above it: the filter threshold; the streaming
 // pass appends every entry at or above it to a shared-memory candidate list (warp-aggregated
 // appends, one shared atomic per warp and 8-entry vector), and a bitonic sort of the
 // candidates by (key, id) gives the answer.  When the sample misleads (fewer than K
@@ -27,18 +27,16 @@ namespace {
 constexpr int kTkThreads = 512;
 constexpr int kTkWarps = kTkThreads / 32;
 constexpr int kSample = 2048;  // sampled keys per row, 4 per thread
-constexpr int kCap = 8192;     // candidates a row may keep
+constexpr int kCap = 4096;     // candidates a row may keep (4 CTAs of 512 threads fit an SM)
 constexpr unsigned kFull = 0xffffffffu;
 
 struct TkSmem {
   unsigned long long cand[kCap];  // (key << 32) | (0xffffffff - id): larger = earlier in the order
-  uint32_t sample[kSample];
   uint32_t hist[256];
   uint32_t warp_sum[kTkWarps];
   uint32_t count;
   uint32_t thr;
   uint32_t need;
-  uint32_t taken;
 };
 
 __device__ __forceinline__ uint32_t key_of_bits(uint32_t u) { return (u & 0x80000000u) ? ~u : (u | 0x80000000u); }
@@ -104,21 +102,31 @@ __device__ __forceinline__ void for_each_key(const E* row, int64_t V, F&& f) {
   constexpr int kVec = 16 / sizeof(E);
   const uintptr_t addr = reinterpret_cast<uintptr_t>(row);
   if (addr % 16 == 0) {
+    // kUnroll 16-byte loads per thread in flight before any is used
+    constexpr int kUnroll = 4;
     const int64_t nvec = V / kVec;
     const uint4* rv = reinterpret_cast<const uint4*>(row);
     const int64_t iters = (nvec + kTkThreads - 1) / kTkThreads;
-    for (int64_t it = 0; it < iters; ++it) {
-      const int64_t v = it * kTkThreads + threadIdx.x;
-      uint4 q = make_uint4(0, 0, 0, 0);
-      const bool ok = v < nvec;
-      if (ok) q = __ldcs(rv + v);
-      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+    for (int64_t it0 = 0; it0 < iters; it0 += kUnroll) {
+      uint4 q[kUnroll];
 #pragma unroll
-      for (int e = 0; e < kVec; ++e) {
-        uint32_t u;
-        if (sizeof(E) == 2) u = (e & 1) ? (w[e >> 1] & 0xffff0000u) : (w[e >> 1] << 16);
-        else u = w[e];
-        f(key_of_bits(u), v * kVec + e, ok);
+      for (int u = 0; u < kUnroll; ++u) {
+        const int64_t v = (it0 + u) * kTkThreads + threadIdx.x;
+        q[u] = v < nvec ? __ldcs(rv + v) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        if (it0 + u >= iters) break;  // the same for the whole CTA
+        const int64_t v = (it0 + u) * kTkThreads + threadIdx.x;
+        const bool ok = v < nvec;
+        const uint32_t w[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+#pragma unroll
+        for (int e = 0; e < kVec; ++e) {
+          uint32_t b;
+          if (sizeof(E) == 2) b = (e & 1) ? (w[e >> 1] & 0xffff0000u) : (w[e >> 1] << 16);
+          else b = w[e];
+          f(key_of_bits(b), v * kVec + e, ok);
+        }
       }
     }
     const int64_t tail0 = nvec * kVec;
@@ -135,6 +143,69 @@ __device__ __forceinline__ void for_each_key(const E* row, int64_t V, F&& f) {
       f(ok ? key_of_bits(bits_at(row, i)) : 0u, i, ok);
     }
   }
+}
+
+// Warp 0 finds, among the 256 bins of sm.hist, the highest bin b such that the bins from
+// 255 down to b hold at least `want` entries; stores b in sm.thr and the count of the bins
+// above b in sm.need.  Every thread calls it (two barriers).
+__device__ __forceinline__ void top_bin(TkSmem& sm, uint32_t want) {
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    // lane l holds bins 255 - 8l .. 248 - 8l (descending)
+    uint32_t c[8], sum = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      c[i] = sm.hist[255 - 8 * lane - i];
+      sum += c[i];
+    }
+    uint32_t incl = sum;  // inclusive scan over lanes (bins from the top)
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const uint32_t excl = incl - sum;
+    const unsigned hit = __ballot_sync(kFull, incl >= want);
+    const int first = hit ? __ffs(hit) - 1 : 31;
+    if (lane == first) {
+      uint32_t cum = excl;
+      int bin = 248 - 8 * lane;
+      for (int i = 0; i < 8; ++i) {
+        if (cum + c[i] >= want) {
+          bin = 255 - 8 * lane - i;
+          break;
+        }
+        cum += c[i];
+      }
+      sm.thr = static_cast<uint32_t>(bin);
+      sm.need = cum;
+    }
+  }
+  __syncthreads();
+}
+
+// The filter threshold from the row's sample (4 keys per thread): the largest key of the
+// form p << 16 with at least `want` sampled keys at or above it (a two-pass radix select
+// on the top 16 key bits; for bf16 rows, whose keys have 16 significant bits, it is the
+// want-th largest sampled key itself).
+__device__ __forceinline__ uint32_t sample_threshold(TkSmem& sm, const uint32_t (&sk)[4], uint32_t want) {
+  for (int b = threadIdx.x; b < 256; b += kTkThreads) sm.hist[b] = 0;
+  __syncthreads();
+#pragma unroll
+  for (int e = 0; e < 4; ++e) atomicAdd(&sm.hist[sk[e] >> 24], 1u);
+  top_bin(sm, want);
+  const uint32_t hi = sm.thr, above = sm.need;
+  __syncthreads();
+  for (int b = threadIdx.x; b < 256; b += kTkThreads) sm.hist[b] = 0;
+  __syncthreads();
+#pragma unroll
+  for (int e = 0; e < 4; ++e)
+    if ((sk[e] >> 24) == hi) atomicAdd(&sm.hist[(sk[e] >> 16) & 255u], 1u);
+  top_bin(sm, want - above);
+  const uint32_t thr = (hi << 24) | (sm.thr << 16);
+  __syncthreads();
+  return thr;
 }
 
 // Exclusive prefix of `flag` over the CTA in thread order: returns this thread's rank and
@@ -169,14 +240,13 @@ __global__ void __launch_bounds__(kTkThreads) topk_kernel(const E* __restrict__ 
   uint32_t thr = 0;  // V <= kCap: keep every entry
   if (V > kCap) {
     const int64_t stride = V / (kSample / 4);
+    uint32_t sk[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) sm.sample[tid * 4 + e] = key_of_bits(bits_at(row, tid * stride + e));
-    __syncthreads();
-    bitonic_desc(sm.sample, kSample);
-    // about 1.5 K + 16 samples' worth of row entries expected at or above the threshold
-    int r = static_cast<int>((3ll * K * kSample + 2 * V - 1) / (2 * V)) + 16;
+    for (int e = 0; e < 4; ++e) sk[e] = key_of_bits(bits_at(row, tid * stride + e));
+    // about 1.5 K + 8 samples' worth of row entries expected at or above the threshold
+    int r = static_cast<int>((3ll * K * kSample + 2 * V - 1) / (2 * V)) + 8;
     if (r > kSample - 1) r = kSample - 1;
-    thr = sm.sample[r];
+    thr = sample_threshold(sm, sk, static_cast<uint32_t>(r) + 1);
   }
   if (tid == 0) sm.count = 0;
   __syncthreads();
