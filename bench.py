@@ -433,9 +433,16 @@ def main():
                 traffic = tj["bytes_per_launch"]
         except (ValueError, KeyError):
             traffic = None
-    roofline = dict(bound="tensor", kernel=dom, achieved=achieved, peak=peak_sust, unit="TFLOP/s",
-                    frac=achieved / peak_sust, traffic=traffic,
-                    peak_note=f"sustained bf16 ({peaks['source']}): kernel timed inside a long step",
+    if cfg.dtype == "f32":
+        # fp32 work runs on the CUDA cores (FFMA): 148 SMs x 128 fp32 lanes x 2 FLOP per clock
+        peak_r, bound, note = 148 * 128 * 2 * peaks.get("sm_max_mhz", 2032.0) / 1e6, "alu", \
+            "fp32 FFMA: 148 SMs x 128 lanes x 2 FLOP x max SM clock"
+    else:
+        peak_r, bound, note = peak_sust, "tensor", \
+            f"sustained bf16 ({peaks['source']}): kernel timed inside a long step"
+    roofline = dict(bound=bound, kernel=dom, achieved=achieved, peak=peak_r, unit="TFLOP/s",
+                    frac=achieved / peak_r, traffic=traffic,
+                    peak_note=note,
                     launches=dom_launches, avg_launch_ms=dom_ms / max(1, dom_launches),
                     share_of_device_time=dom_ms / total_ms if total_ms else None,
                     classes={c: dict(launches=v[0], ms=v[1]) for c, v in per_class.items()})
@@ -465,10 +472,11 @@ def main():
     # ---- CPU baseline: the oracle on a bounded sample, rank 0 at N = 1 only
     cpu = None
     if not args.no_cpu and world == 1 and rank == 0:
+        cpu_rows = min(args.cpu_rows, T)
         rate, secs = cpu_oracle_rate(cfg, h["W"].view(torch.int16).numpy().view(np.uint16)
-                                     if tdt == torch.bfloat16 else h["W"].numpy(), args.cpu_rows)
+                                     if tdt == torch.bfloat16 else h["W"].numpy(), cpu_rows)
         cpu = dict(value=rate, unit="tokens/s", cores=len(os.sched_getaffinity(0)), kind="oracle",
-                   sample=f"oracle fwd+bwd (fp64, full-vocab logit rows, analytic dH/dW) on rows 0..{args.cpu_rows - 1}"
+                   sample=f"oracle fwd+bwd (fp64, full-vocab logit rows, analytic dH/dW) on rows 0..{cpu_rows - 1}"
                           f" of {cfg.name}; {secs:.1f} s")
 
     if rank == 0:
