@@ -27,6 +27,7 @@ PROTOTYPES = {
     "fckl_profile_enable": (None, [ctypes.c_int]),
     "fckl_profile_read": (c_i32, [c_i32, ctypes.POINTER(c_i64), ctypes.POINTER(c_f64), ctypes.c_int]),
     "fckl_debug_gemm_bf16": (c_i32, [c_vp, c_vp, c_vp, c_i64, c_i64, c_i64, c_i32, c_i32, c_i32, c_vp]),
+    "fckl_debug_wait_timeout": (c_i32, [c_vp, c_sz, c_vp]),
     "fckl_topk_extract": (c_i32, [c_vp, c_i64, c_i64, c_i32, c_i32, c_vp, c_vp, c_vp]),
     "fckl_forward_noalloc": (c_i32, [c_vp, c_vp, c_vp, c_vp, c_vp, c_i64, c_i64, c_i64, c_i32, c_f32, c_i64, c_i32,
                                      c_vp, c_vp, c_vp, c_vp, c_vp]),

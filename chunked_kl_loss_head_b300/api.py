@@ -153,6 +153,11 @@ def fckl_profile_read(kernel_class, reset: bool = False):
     return int(n.value), float(ms.value)
 
 
+def fckl_debug_wait_timeout(ws, stream=None):
+    _check(lib().fckl_debug_wait_timeout(_ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "fckl_debug_wait_timeout")
+
+
 def fckl_debug_gemm_bf16(A, B, D, M, N, K, a_mn, b_mn, cta_pair=1, stream=None):
     _check(lib().fckl_debug_gemm_bf16(_ptr(A), _ptr(B), _ptr(D), M, N, K, int(a_mn), int(b_mn), int(cta_pair),
                                       _stream(stream)), "fckl_debug_gemm_bf16")

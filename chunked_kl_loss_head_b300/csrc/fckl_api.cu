@@ -430,6 +430,15 @@ fckl_status fckl_profile_read(int32_t kernel_class, int64_t* launches, double* t
   return FCKL_OK;
 }
 
+fckl_status fckl_debug_wait_timeout(void* ws, size_t ws_bytes, void* stream) {
+  if (!ws || !aligned(ws, kAlign) || ws_bytes < kCtrlBytes) return FCKL_ERR_WORKSPACE;
+  int num_sms = 0;
+  FCKL_TRY(device_info(&num_sms));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  Ctrl* ctrl = reinterpret_cast<Ctrl*>(ws);
+  return step(FCKL_K_OTHER, st, [&] { return tc_debug_wait_timeout(ctrl, st); });
+}
+
 fckl_status fckl_debug_gemm_bf16(const void* A, const void* B, float* D, int64_t M, int64_t N, int64_t K, int32_t a_mn,
                                  int32_t b_mn, int32_t cta_pair, void* stream) {
   if (!A || !B || !D || M < 1 || N < 1 || K < 1) return FCKL_ERR_INVALID_ARG;

@@ -102,6 +102,7 @@ cudaError_t tc_bwd_chunk(const void* Hc, const void* HcT, int64_t ldT, const voi
                          Ctrl* ctrl, void* G, float* dW, int dW_accumulate, float* dH_acc,
                          unsigned int* done_g, unsigned int* done_w, TileSched* sched, int num_sms,
                          cudaStream_t st);
+cudaError_t tc_debug_wait_timeout(Ctrl* ctrl, cudaStream_t st);
 cudaError_t tc_debug_gemm(const void* A, const void* B, float* D, int64_t M, int64_t N, int64_t K,
                           int a_mn, int b_mn, int cta_pair, int num_sms, cudaStream_t st);
 

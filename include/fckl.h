@@ -166,6 +166,12 @@ FCKL_API void fckl_profile_enable(int on);
  * when `reset` is nonzero.  Returns FCKL_ERR_INVALID_ARG for a bad class. */
 FCKL_API fckl_status fckl_profile_read(int32_t kernel_class, int64_t* launches, double* total_ms, int reset);
 
+/* Test hook for the failure path: launches one thread that waits, with the kernels' own
+ * bounded wait, on a barrier nothing arrives on.  After FCKL_WAIT_NS (2 s) the wait gives up
+ * and records FCKL_ERR_TIMEOUT in the workspace's status word, which fckl_get_error then
+ * returns; nothing faults or hangs.  ws: a workspace of at least 256 bytes. */
+FCKL_API fckl_status fckl_debug_wait_timeout(void* ws, size_t ws_bytes, void* stream);
+
 /* Test hook for the tcgen05 GEMM engine: D[M, N] (float32, row-major, ldd = N)
  * = A . B with bf16 operands on the same tensor-core path the loss uses.
  * a_mn == 0: A is [M, K] (K contiguous); a_mn == 1: A is stored [K, M].

@@ -189,3 +189,36 @@ def test_autograd_module_matches_abi():
     assert rel(loss.item(), ref["loss"]) <= 1e-5
     assert rel_max(H.grad.cpu().numpy(), ref["dH"]) <= 1e-4
     assert rel_max(W.grad.cpu().numpy(), ref["dW"]) <= 1e-4
+
+
+def test_autograd_module_bf16():
+    from chunked_kl_loss_head_b300 import FusedChunkedKLLoss
+
+    x = make_small(T=600, d=96, V=3000, K=9, tau=1.2, dtype="bf16", seed=14, mask="random", mask_frac=0.1)
+    d = to_device(x)
+    H = d["H"].clone().requires_grad_(True)
+    W = d["W"].clone().requires_grad_(True)
+    loss = FusedChunkedKLLoss(tau=1.2, chunk=256)(H, W, d["topk_idx"], d["topk_logits"], d["valid"])
+    (0.5 * loss).backward()
+    ref = oracle_of(x, grad=0.5)
+    assert H.grad.dtype == torch.bfloat16 and W.grad.dtype == torch.bfloat16
+    assert rel(loss.item(), ref["loss"]) <= TOL["bf16"]["loss"]
+    assert rel_max(H.grad.float().cpu().numpy(), ref["dH"]) <= TOL["bf16"]["grad"]
+    assert rel_max(W.grad.float().cpu().numpy(), ref["dW"]) <= TOL["bf16"]["grad"]
+
+
+def test_bounded_wait_reports_timeout():
+    """A pipeline wait that never completes gives up after its bound and reports
+    FCKL_ERR_TIMEOUT through the workspace; the device stays usable afterwards."""
+    ws = torch.zeros(4096, dtype=torch.uint8, device="cuda")
+    api.fckl_debug_wait_timeout(ws)
+    assert api.fckl_get_error(ws) == 6  # FCKL_ERR_TIMEOUT
+    assert api.fckl_get_error(ws) == 0  # the read cleared it
+    x = make_small(T=64, d=32, V=300, K=3, tau=1.0, dtype="bf16", seed=31)
+    check(x, run_gpu(x, 64), label="after a timeout")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_largest_k(dtype):
+    x = make_small(T=70, d=64, V=5000, K=1024, tau=1.3, dtype=dtype, seed=32, ids="uniform")
+    check(x, run_gpu(x, 64), label=f"{dtype} K=1024")
