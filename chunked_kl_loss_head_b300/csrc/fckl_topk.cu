@@ -9,8 +9,9 @@
 // One CTA per row, HBM-bound: the row is streamed once.  A strided sample of the row
 // (2048 keys) is radix-selected for a key with r sampled keys above it, r chosen so that
 // a few times K row entries are expected above it: the filter threshold; the streaming
-// pass appends every entry at or above it to a shared-memory candidate list (warp-aggregated
-// appends, one shared atomic per warp and 8-entry vector), and a bitonic sort of the
+// pass appends every entry at or above it to a shared-memory candidate list (per 16-byte
+// vector a warp vote skips vectors without candidates; one shared atomic per warp covers
+// the rest), and a bitonic sort of the
 // candidates by (key, id) gives the answer.  When the sample misleads (fewer than K
 // candidates, or more than the list holds: heavy ties, tiny or adversarial rows) the row
 // takes the exact path: a 4-pass radix select of the K-th largest key, then every entry
@@ -208,6 +209,79 @@ __device__ __forceinline__ uint32_t sample_threshold(TkSmem& sm, const uint32_t 
   return thr;
 }
 
+// The streaming pass of the fast path: appends every entry whose key is >= thr.  Per
+// 16-byte vector each thread builds a bit mask of its passing entries; a warp with no
+// passing entry moves on after one vote, a warp with some takes one shared atomic for all
+// of them (offsets from a warp prefix sum of the lanes' counts).  Rows that do not start
+// on a 16-byte boundary take the generic per-entry walk.
+template <class E>
+__device__ __forceinline__ void scan_append(TkSmem& sm, const E* row, int64_t V, uint32_t thr) {
+  constexpr int kVec = 16 / sizeof(E);
+  constexpr int kUnroll = 4;
+  const uintptr_t addr = reinterpret_cast<uintptr_t>(row);
+  if (addr % 16 != 0) {
+    for_each_key(row, V, [&](uint32_t key, int64_t id, bool ok) { append(sm, ok && key >= thr, key, id); });
+    return;
+  }
+  const int lane = threadIdx.x & 31;
+  const int64_t nvec = V / kVec;
+  const uint4* rv = reinterpret_cast<const uint4*>(row);
+  const int64_t iters = (nvec + kTkThreads - 1) / kTkThreads;
+  for (int64_t it0 = 0; it0 < iters; it0 += kUnroll) {
+    uint4 q[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t v = (it0 + u) * kTkThreads + threadIdx.x;
+      q[u] = v < nvec ? __ldcs(rv + v) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      if (it0 + u >= iters) break;  // the same for the whole CTA
+      const int64_t v = (it0 + u) * kTkThreads + threadIdx.x;
+      const uint32_t w[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+      uint32_t mask = 0;
+      if (v < nvec) {
+#pragma unroll
+        for (int e = 0; e < kVec; ++e) {
+          uint32_t b;
+          if (sizeof(E) == 2) b = (e & 1) ? (w[e >> 1] & 0xffff0000u) : (w[e >> 1] << 16);
+          else b = w[e];
+          mask |= (key_of_bits(b) >= thr ? 1u : 0u) << e;
+        }
+      }
+      if (!__any_sync(kFull, mask != 0)) continue;
+      const uint32_t cnt = static_cast<uint32_t>(__popc(mask));
+      uint32_t incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += y;
+      }
+      uint32_t base = 0;
+      if (lane == 31) base = atomicAdd(&sm.count, incl);
+      base = __shfl_sync(kFull, base, 31) + incl - cnt;
+      while (mask) {
+        const int e = __ffs(mask) - 1;
+        mask &= mask - 1;
+        const int c = sizeof(E) == 2 ? e >> 1 : e;  // the 32-bit word holding entry e (selects, no local array)
+        const uint32_t word = c == 0 ? q[u].x : c == 1 ? q[u].y : c == 2 ? q[u].z : q[u].w;
+        uint32_t b;
+        if (sizeof(E) == 2) b = (e & 1) ? (word & 0xffff0000u) : (word << 16);
+        else b = word;
+        if (base < static_cast<uint32_t>(kCap)) sm.cand[base] = composite(key_of_bits(b), v * kVec + e);
+        ++base;
+      }
+    }
+  }
+  const int64_t tail0 = nvec * kVec;
+  if (tail0 < V) {
+    const int64_t i = tail0 + threadIdx.x;
+    const bool ok = i < V;
+    const uint32_t key = ok ? key_of_bits(bits_at(row, i)) : 0u;
+    append(sm, ok && key >= thr, key, i);
+  }
+}
+
 // Exclusive prefix of `flag` over the CTA in thread order: returns this thread's rank and
 // the CTA total through `total` (the same for every thread).
 __device__ __forceinline__ uint32_t cta_rank(TkSmem& sm, bool flag, uint32_t* total) {
@@ -250,7 +324,7 @@ __global__ void __launch_bounds__(kTkThreads) topk_kernel(const E* __restrict__ 
   }
   if (tid == 0) sm.count = 0;
   __syncthreads();
-  for_each_key(row, V, [&](uint32_t key, int64_t id, bool ok) { append(sm, ok && key >= thr, key, id); });
+  scan_append(sm, row, V, thr);
   __syncthreads();
   uint32_t n = sm.count;
   bool exact = n < static_cast<uint32_t>(K) || n > static_cast<uint32_t>(kCap);
