@@ -744,16 +744,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t b_desc0 = q.b_mn ? sdesc_sw128(smem_u32(sB), 8192, 1024) : sdesc_sw128(smem_u32(sB), 16, 1024);
         const uint64_t a_kstep = q.a_mn ? 2048 >> 4 : 32 >> 4, b_kstep = q.b_mn ? 2048 >> 4 : 32 >> 4;
         const int n_stages = (tr.num_k + S::KSUB - 1) / S::KSUB;
-        // The issuing thread runs in step with the tensor pipe (an MMA is accepted only as
-        // the previous one drains), so anything it does between two MMAs is a bubble.  The
-        // wait for stage kb+1 is therefore made before the last MMA of stage kb, while the
-        // MMA before it executes.
-        bool ok = wait_or_abort(&full[it % S::STAGES], (it / S::STAGES) & 1, af, ctrl);
-        if (ok) tc_fence_after();
-        for (int kb = 0; ok && kb < n_stages; ++kb, ++it) {
+        bool ok = true;
+        for (int kb = 0; kb < n_stages; ++kb, ++it) {
           const int s = it % S::STAGES;
+          const uint32_t ph = (it / S::STAGES) & 1;
+          if (!wait_or_abort(&full[s], ph, af, ctrl)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
           const int nsub = tr.num_k - kb * S::KSUB < S::KSUB ? tr.num_k - kb * S::KSUB : S::KSUB;
-          const bool more = kb + 1 < n_stages;
 #pragma unroll
           for (int j = 0; j < S::KSUB; ++j) {
             if (j < nsub) {
@@ -761,10 +761,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint64_t bd = b_desc0 + static_cast<uint64_t>((s * S::B_BYTES + j * S::B_SUB) >> 4);
 #pragma unroll
               for (int k = 0; k < BK / 16; ++k) {
-                if (j == nsub - 1 && k == BK / 16 - 1 && more) {
-                  if (!wait_or_abort(&full[(it + 1) % S::STAGES], ((it + 1) / S::STAGES) & 1, af, ctrl)) ok = false;
-                  else tc_fence_after();
-                }
                 if (CG == 2) umma_f16_pair(d_tmem, ad + k * a_kstep, bd + k * b_kstep, idesc, (kb | j | k) != 0);
                 else umma_f16(d_tmem, ad + k * a_kstep, bd + k * b_kstep, idesc, (kb | j | k) != 0);
               }
