@@ -222,3 +222,21 @@ def test_bounded_wait_reports_timeout():
 def test_largest_k(dtype):
     x = make_small(T=70, d=64, V=5000, K=1024, tau=1.3, dtype=dtype, seed=32, ids="uniform")
     check(x, run_gpu(x, 64), label=f"{dtype} K=1024")
+
+
+@pytest.mark.parametrize("case", range(24))
+def test_random_shapes(case):
+    """Seeded random small shapes across both paths: ragged T, d (a multiple of 8 for
+    bf16), V, K, tau and chunk, random masks, some near-one-hot teachers."""
+    rng = np.random.default_rng(1000 + case)
+    dtype = "bf16" if case % 3 else "f32"
+    T = int(rng.integers(1, 1500))
+    d = int(rng.integers(1, 48)) * 8
+    V = int(rng.integers(16, 9000))
+    K = int(min(V, rng.choice([1, 2, 5, 17, 64])))
+    tau = float(rng.choice([0.5, 1.0, 1.7, 3.0]))
+    chunk = int(rng.choice([1, 7, 64, 128, 300, 1000, 4096]))
+    x = make_small(T=T, d=d, V=V, K=K, tau=tau, dtype=dtype, seed=case, ids="uniform" if case % 2 else "zipf",
+                   mask="random", mask_frac=float(rng.choice([0.0, 0.1, 0.5])),
+                   onehot_frac=float(rng.choice([0.0, 0.2])), logit_offset=10.0)
+    check(x, run_gpu(x, chunk), label=f"random {case}: {dtype} T={T} d={d} V={V} K={K} tau={tau} chunk={chunk}")
