@@ -380,14 +380,64 @@ __global__ void __launch_bounds__(kTkThreads) topk_kernel(const E* __restrict__ 
     __syncthreads();
   }
 
-  // ---- sort the candidates (padded with zeros, which sort last) and write the first K
+  // ---- narrow the candidates to about K before sorting: the 16-bit key prefix of the K-th
+  // largest candidate (a two-pass radix select over the list) bounds what can be in the
+  // answer; the candidates at or above it move to the upper half of the list and only
+  // they are sorted.  (For bf16 rows, whose keys have 16 significant bits, they are the K
+  // answers plus any ties with the K-th.)  When they would not fit, the whole list is sorted.
+  unsigned long long* srt = sm.cand;
+  if (n > static_cast<uint32_t>(K) && n <= static_cast<uint32_t>(kCap / 2)) {
+    for (int b = tid; b < 256; b += kTkThreads) sm.hist[b] = 0;
+    __syncthreads();
+    for (int i = tid; i < static_cast<int>(n); i += kTkThreads)
+      atomicAdd(&sm.hist[static_cast<uint32_t>(sm.cand[i] >> 56)], 1u);
+    top_bin(sm, static_cast<uint32_t>(K));
+    const uint32_t hi = sm.thr, above = sm.need;
+    __syncthreads();
+    for (int b = tid; b < 256; b += kTkThreads) sm.hist[b] = 0;
+    __syncthreads();
+    for (int i = tid; i < static_cast<int>(n); i += kTkThreads) {
+      const uint32_t key = static_cast<uint32_t>(sm.cand[i] >> 32);
+      if ((key >> 24) == hi) atomicAdd(&sm.hist[(key >> 16) & 255u], 1u);
+    }
+    top_bin(sm, static_cast<uint32_t>(K) - above);
+    const uint32_t cut = (hi << 24) | (sm.thr << 16);
+    if (tid == 0) sm.count = 0;
+    __syncthreads();
+    const int rounds = (static_cast<int>(n) + kTkThreads - 1) / kTkThreads;
+    for (int r = 0; r < rounds; ++r) {
+      const int i = r * kTkThreads + tid;
+      const unsigned long long c = i < static_cast<int>(n) ? sm.cand[i] : 0ull;
+      const bool keep = i < static_cast<int>(n) && static_cast<uint32_t>(c >> 32) >= cut;
+      const unsigned m = __ballot_sync(kFull, keep);
+      if (m) {
+        const int lane = tid & 31, leader = __ffs(m) - 1;
+        uint32_t base = 0;
+        if (lane == leader) base = atomicAdd(&sm.count, static_cast<uint32_t>(__popc(m)));
+        base = __shfl_sync(kFull, base, leader);
+        if (keep) {
+          const uint32_t pos = base + static_cast<uint32_t>(__popc(m & ((1u << lane) - 1u)));
+          if (pos < static_cast<uint32_t>(kCap / 2)) sm.cand[kCap / 2 + pos] = c;
+        }
+      }
+    }
+    __syncthreads();
+    const uint32_t kept = sm.count;
+    __syncthreads();
+    if (kept >= static_cast<uint32_t>(K) && kept <= static_cast<uint32_t>(kCap / 2)) {
+      srt = sm.cand + kCap / 2;
+      n = kept;
+    }
+  }
+
+  // ---- sort (padded with zeros, which sort last) and write the first K
   int np2 = 1;
   while (np2 < static_cast<int>(n)) np2 <<= 1;
-  for (int i = static_cast<int>(n) + tid; i < np2; i += kTkThreads) sm.cand[i] = 0ull;
+  for (int i = static_cast<int>(n) + tid; i < np2; i += kTkThreads) srt[i] = 0ull;
   __syncthreads();
-  bitonic_desc(sm.cand, np2);
+  bitonic_desc(srt, np2);
   for (int k = tid; k < K; k += kTkThreads) {
-    const unsigned long long c = sm.cand[k];
+    const unsigned long long c = srt[k];
     const uint32_t key = static_cast<uint32_t>(c >> 32);
     out_idx[t * K + k] = static_cast<int32_t>(0xffffffffu - static_cast<uint32_t>(c & 0xffffffffull));
     out_val[t * K + k] = __uint_as_float(bits_of_key(key));
