@@ -271,8 +271,9 @@ __device__ __forceinline__ float pick32(const uint32_t (&v)[32], int j) {
 // 128-row block of the result that this CTA holds.  tcgen05.ld is warp-collective, so
 // loops over columns are uniform across the warp and only the memory traffic is predicated
 // on the row.  done() is called once per tile by one epilogue thread after all four
-// epilogue warps of the CTA have finished it (only when kSignals), with their global
-// stores fenced at GPU scope and toward the async proxy.
+// epilogue warps of the CTA have finished it (only when kSignals); before it, lane 0 of
+// each of those warps has called settle() (wait for whatever of the warp's writes the
+// signal must cover) and fenced toward the async proxy and at GPU scope.
 
 // Forward logit tile (256 vocab columns): per-row (max, sum) of exp2(z * log2e / tau)
 // over the tile's columns, and z at every teacher id that falls in the tile.
@@ -334,10 +335,20 @@ struct FwdEpi {
   __device__ __forceinline__ void done(const TileRef&) const {}
 };
 
+// Staging shared memory of the TMA epilogues: per epilogue warp two 4 KB buffers, each
+// holding a 32-row block of 128-byte rows.
+constexpr int kWarpStaging = 2 * 32 * 128;
+constexpr int kEpiStaging = 4 * kWarpStaging;
+
 // Backward logit tile of vocab stripe s (columns [s0, s0 + S) with s0 = s * S):
 // G = (exp(s - lse) - p) * alpha, alpha = g / (tau N) for valid rows and 0 for ignored
 // rows, stored as bf16 into gradient buffer s % 3 (columns [buf * S, buf * S + S) of the
 // [rows, ldG] buffer, ldG = 3 * S).  Columns at or past V are written as zeros.
+// Each epilogue warp owns 32 rows; per 64-column chunk it converts two 32-column TMEM
+// loads to bf16, writes the 32 x 64 block (32 rows of 128 bytes, 128-byte swizzle) into
+// one of its two 4 KB staging buffers and one lane TMA-stores it through the output map
+// (the gradient buffer, 64 x 32 boxes, rows past the chunk clipped).  Whole 128-byte row
+// segments then reach L2 from one bulk copy instead of 16-byte stores from every thread.
 struct BwdEpi {
   int64_t rows, V, S, ldG;
   float c2;
@@ -347,18 +358,20 @@ struct BwdEpi {
   const float* lse;
   const uint8_t* valid;
   Ctrl* ctrl;
-  __nv_bfloat16* G;
 
-  __device__ __forceinline__ void run(const TileRef& tr, uint32_t taddr, int m_blk, int r, const EpiCtx&,
-                                      uint32_t&) const {
+  __device__ __forceinline__ void run(const TileRef& tr, uint32_t taddr, int m_blk, int r, const EpiCtx& cx,
+                                      uint32_t& seq) const {
+    const int lane = r & 31, quad = r >> 5;
     const int64_t row = static_cast<int64_t>(m_blk) * BM + r;
+    const int64_t m0 = static_cast<int64_t>(m_blk) * BM + quad * 32;  // this warp's first row
     const bool live = row < rows;
     const int64_t s0 = static_cast<int64_t>(tr.stripe) * S;
     const int BN = tr.bn;
     const int64_t n0l = tr.n0;
     const int64_t n0 = s0 + n0l;
     const int64_t vend = (s0 + S < V) ? s0 + S : V;
-    __nv_bfloat16* Gb = G + (tr.stripe % kGradBuffers) * S;
+    const int64_t xbuf = (tr.stripe % kGradBuffers) * S + n0l;  // buffer column of the tile
+    uint8_t* wbuf = cx.staging + quad * kWarpStaging;
     float lse2 = 0.f, a = 0.f;
     const int32_t* ids = sidx + (live ? row : 0) * K;
     int k = K;
@@ -369,36 +382,58 @@ struct BwdEpi {
     }
     int64_t nid = (k < K) ? ids[k] : INT64_MAX;
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 32) {
+    for (int c = 0; c < BN; c += 64) {
       if (n0l + c >= S) break;
-      uint32_t v[32];
-      tmem_ld_32x32(taddr + c, v);
-      tmem_ld_wait();
-      float g[32];
+      uint8_t* buf = wbuf + (seq & 1) * (32 * 128);
+      ++seq;
+      if (lane == 0) bulk_wait_read<1>();  // the copy issued two chunks ago has read `buf`
+      __syncwarp();
+      uint8_t* rowp = buf + lane * 128;
 #pragma unroll
-      for (int i = 0; i < 32; ++i)
-        g[i] = (n0 + c + i < vend) ? exp2f(__uint_as_float(v[i]) * c2 - lse2) : 0.f;
-      while (nid < n0 + c + 32) {
-        const int j = static_cast<int>(nid - (n0 + c));
-        const float pk = sp[row * K + k];
+      for (int h = 0; h < 2; ++h) {
+        const int64_t nc = n0 + c + 32 * h;  // vocab column of this 32-column half
+        float g[32];
+        if (c + 32 * h < BN) {
+          uint32_t v[32];
+          tmem_ld_32x32(taddr + c + 32 * h, v);
+          tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) g[i] -= (i == j) ? pk : 0.f;
-        ++k;
-        nid = (k < K) ? ids[k] : INT64_MAX;
-      }
-      if (live) {
+          for (int i = 0; i < 32; ++i) g[i] = (nc + i < vend) ? exp2f(__uint_as_float(v[i]) * c2 - lse2) : 0.f;
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) g[i] = 0.f;
+        }
+        while (nid < nc + 32) {
+          const int j = static_cast<int>(nid - nc);
+          const float pk = sp[row * K + k];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) g[i] -= (i == j) ? pk : 0.f;
+          ++k;
+          nid = (k < K) ? ids[k] : INT64_MAX;
+        }
         uint32_t w[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          __nv_bfloat162 h = __floats2bfloat162_rn(g[2 * i] * a, g[2 * i + 1] * a);
-          w[i] = *reinterpret_cast<uint32_t*>(&h);
+          __nv_bfloat162 b2 = __floats2bfloat162_rn(g[2 * i] * a, g[2 * i + 1] * a);
+          w[i] = *reinterpret_cast<uint32_t*>(&b2);
         }
-        uint4* dst = reinterpret_cast<uint4*>(Gb + row * ldG + n0l + c);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) dst[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+        for (int q = 0; q < 4; ++q) {
+          const int piece = 4 * h + q;
+          *reinterpret_cast<uint4*>(rowp + ((piece ^ (lane & 7)) << 4)) =
+              make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0 && m0 < rows) {
+        tma_store_2d(cx.out, buf, static_cast<int32_t>(xbuf + c), static_cast<int32_t>(m0));
+        bulk_commit();
       }
     }
   }
+
+  __device__ __forceinline__ void done(const TileRef&) const {}
 };
 
 // fp32 result tile through TMA.  Each epilogue warp owns 32 rows of the tile; per
@@ -416,8 +451,7 @@ struct F32Epi {
   int64_t y_stripe;  // rows of the output per vocab stripe (0: no shift)
   Ctrl* ctrl;
 
-  static constexpr int kWarpStaging = 2 * 32 * 32 * 4;
-  static constexpr int kStaging = 4 * kWarpStaging;
+  static constexpr int kStaging = kEpiStaging;
   static constexpr int kKSub = 2;
   static constexpr bool kSignals = false;
 
@@ -476,9 +510,9 @@ struct F32Epi {
 //   a G tile of stripe s >= 3 overwrites the buffer of stripe s - 3: it waits for all
 //   dH^T and dW tiles of stripe s - 3.
 // The producers of both CTAs of a pair wait on the counters (acquire, then a proxy fence
-// so that their TMA reads see the G written by other CTAs' plain stores); each CTA adds
-// one to its stripe's counter when its epilogue has finished a tile (release, after a
-// proxy fence).
+// before their TMA reads of G); each CTA adds one to its stripe's counter when its
+// epilogue has finished a tile (release).  For a G tile every epilogue warp first waits
+// until its TMA stores of the tile have completed (settle), so the count covers them.
 struct BwdChunkEpi {
   BwdEpi g;
   F32Epi h, w;
@@ -486,7 +520,7 @@ struct BwdChunkEpi {
   unsigned int* done_g;
   unsigned int* done_w;
 
-  static constexpr int kStaging = F32Epi::kStaging;
+  static constexpr int kStaging = kEpiStaging;
   static constexpr int kKSub = 2;
   static constexpr bool kSignals = true;
 
@@ -495,6 +529,10 @@ struct BwdChunkEpi {
     if (tr.prob == 0) g.run(tr, taddr, m_blk, r, cx, seq);
     else if (tr.prob == 1) h.run(tr, taddr, m_blk, r, cx, seq);
     else w.run(tr, taddr, m_blk, r, cx, seq);
+  }
+
+  __device__ __forceinline__ void settle(const TileRef& tr) const {
+    if (tr.prob == 0) bulk_wait<0>();
   }
 
   __device__ __forceinline__ void done(const TileRef& tr) const {
@@ -807,14 +845,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const EpiCtx cx{&maps.o[tr.prob], staging};
       epi.run(tr, taddr, m_blk, r, cx, seq);
       tc_fence_before();
-      if (Epi::kSignals) {
+      if constexpr (Epi::kSignals) {
         // The last of the four epilogue warps through this tile reports it done.  Each warp
         // counts before it releases the accumulator, so no warp can reach the next use of
-        // the same counter (two tiles later) before all four have counted this one; nothing
-        // here waits.
-        fence_proxy_async_global();
+        // the same counter (two tiles later) before all four have counted this one.  The
+        // only wait is settle(): for the warp's own bulk writes of the tile to land.
         __syncwarp();
         if (lane == 0) {
+          epi.settle(tr);
+          fence_proxy_async_global();
           __threadfence();
           const uint32_t seen = atomicAdd(&epi_count[acc], 1u);
           if (seen == kEpiWarps * use + kEpiWarps - 1) epi.done(tr);
@@ -1046,9 +1085,9 @@ cudaError_t tc_bwd_chunk(const void* Hc, const void* HcT, int64_t ldT, const voi
   if (!map_kmajor(&maps.a[0], Hc, d, rows, d, BM) || !map_kmajor(&maps.b[0], W, d, V, d, kTileV / cg) ||
       !map_mnmajor(&maps.a[1], W, d, V, d) || !map_kmajor(&maps.b[1], G, ldG, rows, ldG, bn_h / cg) ||
       !map_mnmajor(&maps.a[2], G, ldG, rows, ldG) || !map_kmajor(&maps.b[2], HcT, rows, d, ldT, bn_w / cg) ||
+      !encode_tmap_bf16_2d(&maps.o[0], G, ldG, rows, ldG * 2, 64, 32) ||
       !map_out_f32(&maps.o[1], dH_acc, d, rows, d) || !map_out_f32(&maps.o[2], dW, d, V, d))
     return cudaErrorInvalidValue;
-  maps.o[0] = maps.o[1];
   const Prob p[3] = {make_prob(rows, S, d, kTileV, false, false, false, cg),
                      make_prob(d, rows, S, bn_h, true, false, true, cg),
                      make_prob(S, d, rows, bn_w, true, false, true, cg)};
@@ -1060,7 +1099,7 @@ cudaError_t tc_bwd_chunk(const void* Hc, const void* HcT, int64_t ldT, const voi
   g.done_g = done_g;
   g.done_w = done_w;
   BwdChunkEpi e;
-  e.g = BwdEpi{rows, V, S, ldG, kLog2e / tau, sidx, sp, K, lse, valid, ctrl, static_cast<__nv_bfloat16*>(G)};
+  e.g = BwdEpi{rows, V, S, ldG, kLog2e / tau, sidx, sp, K, lse, valid, ctrl};
   e.h = F32Epi{d, rows, 1, 1, 0, ctrl};
   e.w = F32Epi{S, d, dW_accumulate, 0, S, ctrl};
   e.ctrl = ctrl;
