@@ -164,11 +164,39 @@ def run_reference(args, cfg):
     print(json.dumps(line), flush=True)
 
 
+def dense_torch_step(H, W, idx, tl, valid, tau):
+    """The loss the plain way, for comparison only: build the [T, V] student logits with one
+    bf16 matmul, log-softmax them in fp32, gather at the teacher's ids and let autograd
+    produce dH and dW.  Plain PyTorch ops on the GPU, none of this library's kernels.
+    Returns (loss, dH, dW)."""
+    import torch
+
+    Hl = H.detach().requires_grad_(True)
+    Wl = W.detach().requires_grad_(True)
+    z = Hl @ Wl.t()
+    logq = torch.log_softmax(z.float() / tau, dim=-1)
+    logp = torch.log_softmax(tl.float() / tau, dim=-1)
+    row = (logp.exp() * (logp - logq.gather(1, idx.long()))).sum(1)
+    v = valid.float()
+    loss = (row * v).sum() / v.sum().clamp(min=1.0)
+    loss.backward()
+    return loss.detach(), Hl.grad, Wl.grad
+
+
+# Bytes per [T x V] element the dense path holds at its peak, rounded up: at 8K and 32K
+# tokens of the gpt-oss vocabulary its measured peak is 14 bytes per logit (the fp32
+# log-softmax kept for backward plus, in backward, fp32 gradients and a bf16 cast).
+DENSE_BYTES_PER_ELEM = 16
+
+
 def run_memory_curve(args, cfg):
     """Peak device memory of one fused fwd+bwd (inputs, outputs and workspace included) as
     the token count grows, next to the size of the one dense [T x V] bf16 tensor the
-    method never builds (the pages' isolated loss benchmark compares memory this way,
-    axbrief.com, "Quantifying the Efficiency Gain: 15.6x VRAM Reduction")."""
+    method never builds, and the same step done the dense way in plain PyTorch (peak
+    memory, time, loss) where it fits: the pages' isolated loss benchmark compares the two
+    this way (axbrief.com, "Quantifying the Efficiency Gain: 15.6x VRAM Reduction").  A
+    dense point whose predicted peak exceeds 80% of the free device memory is not run (no
+    out-of-memory attempts); its prediction is reported instead."""
     import torch
 
     from chunked_kl_loss_head_b300 import api
@@ -205,14 +233,53 @@ def run_memory_curve(args, cfg):
             raise SystemExit(f"device status: {api.fckl_status_string(status)}")
         peak = torch.cuda.max_memory_allocated(dev)
         free1, _ = torch.cuda.mem_get_info(dev)
-        points.append(dict(T=T, peak_device_gib=peak / 2 ** 30,
-                           nontorch_device_gib=max(0.0, (free0 - free1 - peak) / 2 ** 30),
-                           workspace_gib=ws.numel() / 2 ** 30, loss=float(loss.item()),
-                           dense_TxV_bf16_gib=dense_logit_bytes(T, c.V) / 2 ** 30))
-        del g, ws, loss, lse, dH, dW
+        fused_ms = time_ms(lambda: (api.forward(g["H"], g["W"], g["topk_idx"], g["topk_logits"], g["valid"],
+                                                c.tau, chunk, ws=ws)[1],
+                                    api.backward(g["H"], g["W"], g["topk_idx"], g["topk_logits"], g["valid"],
+                                                 lse, c.tau, chunk, ws=ws)), dev)
+        pt = dict(T=T, peak_device_gib=peak / 2 ** 30,
+                  nontorch_device_gib=max(0.0, (free0 - free1 - peak) / 2 ** 30),
+                  workspace_gib=ws.numel() / 2 ** 30, loss=float(loss.item()), fused_ms=fused_ms,
+                  dense_TxV_bf16_gib=dense_logit_bytes(T, c.V) / 2 ** 30)
+        del ws, loss, lse, dH, dW
+        if not args.no_dense:
+            base = torch.cuda.memory_allocated(dev)
+            predicted = base + DENSE_BYTES_PER_ELEM * T * c.V
+            torch.cuda.empty_cache()
+            free2, _ = torch.cuda.mem_get_info(dev)
+            pt["dense_predicted_gib"] = predicted / 2 ** 30
+            if predicted - base > 0.8 * free2:
+                pt["dense"] = "not run: predicted peak above 80% of free device memory"
+            else:
+                torch.cuda.reset_peak_memory_stats(dev)
+                dl, _, _ = dense_torch_step(g["H"], g["W"], g["topk_idx"], g["topk_logits"], g["valid"], c.tau)
+                torch.cuda.synchronize(dev)
+                pt["dense_peak_device_gib"] = torch.cuda.max_memory_allocated(dev) / 2 ** 30
+                pt["dense_loss"] = float(dl.item())
+                pt["dense_ms"] = time_ms(lambda: dense_torch_step(g["H"], g["W"], g["topk_idx"], g["topk_logits"],
+                                                                  g["valid"], c.tau), dev)
+        points.append(pt)
+        del g
+        torch.cuda.empty_cache()
     print(json.dumps(dict(metric="peak device GiB of one fused fwd+bwd vs tokens", unit="GiB",
                           config=dict(workload=cfg.name, d=cfg.d, V=cfg.V, K=cfg.K, chunk=chunk),
                           points=points)), flush=True)
+
+
+def time_ms(fn, dev, reps=3):
+    """Mean device time of fn() over `reps` runs after one warm-up, with CUDA events on the
+    current stream."""
+    import torch
+
+    fn()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize(dev)
+    return e0.elapsed_time(e1) / reps
 
 
 def run_topk(args, cfg):
@@ -291,6 +358,7 @@ def main():
     ap.add_argument("--topk-rows", type=int, default=4096, help="rows of the --path topk workload")
     ap.add_argument("--path", default="loss", choices=["loss", "topk"],
                     help="topk: time the teacher top-K extraction instead (one JSON line)")
+    ap.add_argument("--no-dense", action="store_true", help="--memory-curve without the dense PyTorch arm")
     ap.add_argument("--memory-curve", default="",
                     help="comma-separated token counts: peak device memory of one fwd+bwd of the workload's "
                          "shape at each T (one JSON line), instead of the timing run")

@@ -652,6 +652,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t full_leader0 = CG == 2 ? remote(&full[0], 0) : 0u;
       const unsigned int g_target = static_cast<unsigned int>(CG * g.p[0].tiles);
       const unsigned int w_target = static_cast<unsigned int>(CG * (g.p[1].tiles + g.p[2].tiles));
+      // The next tile index is fetched one tile ahead, so the counter's round trip overlaps
+      // the current tile's loads instead of delaying the next tile's first stage.
+      auto fetch = [&]() -> int {
+        if (g.counter) return static_cast<int>(atomicAdd(g.counter, 1u) - g.base);
+        const int v = next_static;
+        next_static += units;
+        return v;
+      };
+      int pre = leader ? fetch() : 0;
+      // Stripes whose dependency counters this producer has already seen complete (chunk
+      // backward): consecutive tiles of one stripe check once.
+      int seen_g = -1, seen_w = -1;
       for (int i = 0;; ++i) {
         const int slot = i % kQueue;
         const uint32_t qph = (i / kQueue) & 1;
@@ -660,16 +672,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (leader) {
           if (!wait_or_abort(&qempty[slot], qph ^ 1, af, ctrl)) break;
           for (;;) {
-            if (g.counter) {
-              t = static_cast<int>(atomicAdd(g.counter, 1u) - g.base);
-            } else {
-              t = next_static;
-              next_static += units;
-            }
+            t = pre;
             if (t >= g.tiles) {
               t = -1;
               break;
             }
+            pre = fetch();
             tr = tile_of<CG>(g, t);
             if (!tr.skip) break;
             // nothing to compute: count it for both CTAs of the pair
@@ -692,9 +700,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           // chunk backward: the tile's inputs (G of its stripe) or its output buffer (the
           // stripe three back) must be ready
           bool ok = true;
-          if (tr.prob != 0) ok = wait_counter(&g.done_g[tr.stripe], g_target, af, ctrl);
-          else if (tr.stripe >= kGradBuffers)
+          if (tr.prob != 0) {
+            if (tr.stripe != seen_g) {
+              ok = wait_counter(&g.done_g[tr.stripe], g_target, af, ctrl);
+              seen_g = tr.stripe;
+            }
+          } else if (tr.stripe >= kGradBuffers && tr.stripe - kGradBuffers != seen_w) {
             ok = wait_counter(&g.done_w[tr.stripe - kGradBuffers], w_target, af, ctrl);
+            seen_w = tr.stripe - kGradBuffers;
+          }
           if (!ok) break;
           fence_proxy_async_global();
         }
