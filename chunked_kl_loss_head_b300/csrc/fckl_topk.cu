@@ -9,10 +9,10 @@
 // One CTA per row, HBM-bound: the row is streamed once.  A strided sample of the row
 // (2048 keys) is radix-selected for a key with r sampled keys above it, r chosen so that
 // a few times K row entries are expected above it: the filter threshold; the streaming
-// pass appends every entry at or above it to a shared-memory candidate list (per 16-byte
-// vector a warp vote skips vectors without candidates; one shared atomic per warp covers
-// the rest), and a bitonic sort of the
-// candidates by (key, id) gives the answer.  When the sample misleads (fewer than K
+// pass appends every entry at or above it to a shared-memory candidate list (a 16-byte
+// vector is ruled out by one signed max of its raw bits; a thread whose vector has
+// candidates takes one shared atomic for them), and a bitonic sort of the candidates,
+// first narrowed to about K, by (key, id) gives the answer.  When the sample misleads (fewer than K
 // candidates, or more than the list holds: heavy ties, tiny or adversarial rows) the row
 // takes the exact path: a 4-pass radix select of the K-th largest key, then every entry
 // above it plus the entries equal to it in id order.
@@ -209,11 +209,66 @@ __device__ __forceinline__ uint32_t sample_threshold(TkSmem& sm, const uint32_t 
   return thr;
 }
 
-// The streaming pass of the fast path: appends every entry whose key is >= thr.  Per
-// 16-byte vector each thread builds a bit mask of its passing entries; a warp with no
-// passing entry moves on after one vote, a warp with some takes one shared atomic for all
-// of them (offsets from a warp prefix sum of the lanes' counts).  Rows that do not start
-// on a 16-byte boundary take the generic per-entry walk.
+// Bit e set when entry e of the 16-byte vector q passes key >= thr.  When the threshold
+// is at or above the key of +0 (the usual case: it sits among the row's largest logits),
+// that test is a signed compare of the raw bits against the threshold's value bits:
+// negative values and negative NaNs have negative patterns, and positive NaNs sort above
+// +inf in both orders.  One signed max over the vector then rules out the vectors with no
+// passing entry, nearly all of them.  (A bf16 threshold has zero low 16 bits, so a word's
+// high entry can be compared without masking off the low one.)  Below +0 the
+// order-preserving keys are compared entry by entry.
+template <class E>
+__device__ __forceinline__ uint32_t vec_hits(const uint4& q, uint32_t thr) {
+  constexpr int kVec = 16 / sizeof(E);
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+  uint32_t mask = 0;
+  if (thr >= 0x80000000u) {
+    const int32_t T = static_cast<int32_t>(thr & 0x7fffffffu);
+    int32_t m = max(max(static_cast<int32_t>(q.x), static_cast<int32_t>(q.y)),
+                    max(static_cast<int32_t>(q.z), static_cast<int32_t>(q.w)));
+    if (sizeof(E) == 2)
+      m = max(m, max(max(static_cast<int32_t>(q.x << 16), static_cast<int32_t>(q.y << 16)),
+                     max(static_cast<int32_t>(q.z << 16), static_cast<int32_t>(q.w << 16))));
+    if (m < T) return 0;
+#pragma unroll
+    for (int e = 0; e < kVec; ++e) {
+      const uint32_t bits = (sizeof(E) == 2 && !(e & 1)) ? (w[e >> 1] << 16) : w[sizeof(E) == 2 ? e >> 1 : e];
+      mask |= (static_cast<int32_t>(bits) >= T ? 1u : 0u) << e;
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < kVec; ++e) {
+      uint32_t bits;
+      if (sizeof(E) == 2) bits = (e & 1) ? (w[e >> 1] & 0xffff0000u) : (w[e >> 1] << 16);
+      else bits = w[e];
+      mask |= (key_of_bits(bits) >= thr ? 1u : 0u) << e;
+    }
+  }
+  return mask;
+}
+
+// Appends the entries of vector q flagged in `mask` (ids id0, id0 + 1, ...): one shared
+// atomic per thread with hits (at the gpt-oss shape about one vector in 25 has any).
+template <class E>
+__device__ __forceinline__ void append_vec(TkSmem& sm, const uint4& q, uint32_t mask, int64_t id0) {
+  uint32_t base = atomicAdd(&sm.count, static_cast<uint32_t>(__popc(mask)));
+  while (mask) {
+    const int e = __ffs(mask) - 1;
+    mask &= mask - 1;
+    const int wi = sizeof(E) == 2 ? e >> 1 : e;  // the 32-bit word holding entry e (selects, no local array)
+    const uint32_t word = wi == 0 ? q.x : wi == 1 ? q.y : wi == 2 ? q.z : q.w;
+    uint32_t bits;
+    if (sizeof(E) == 2) bits = (e & 1) ? (word & 0xffff0000u) : (word << 16);
+    else bits = word;
+    if (base < static_cast<uint32_t>(kCap)) sm.cand[base] = composite(key_of_bits(bits), id0 + e);
+    ++base;
+  }
+}
+
+// The streaming pass of the fast path: appends every entry whose key is >= thr.  Each
+// thread keeps four 16-byte loads in flight, then filters the four vectors (vec_hits) and
+// appends the few passing entries (append_vec).  Rows that do not start on a 16-byte
+// boundary take the generic per-entry walk.
 template <class E>
 __device__ __forceinline__ void scan_append(TkSmem& sm, const E* row, int64_t V, uint32_t thr) {
   constexpr int kVec = 16 / sizeof(E);
@@ -223,7 +278,6 @@ __device__ __forceinline__ void scan_append(TkSmem& sm, const E* row, int64_t V,
     for_each_key(row, V, [&](uint32_t key, int64_t id, bool ok) { append(sm, ok && key >= thr, key, id); });
     return;
   }
-  const int lane = threadIdx.x & 31;
   const int64_t nvec = V / kVec;
   const uint4* rv = reinterpret_cast<const uint4*>(row);
   const int64_t iters = (nvec + kTkThreads - 1) / kTkThreads;
@@ -238,38 +292,9 @@ __device__ __forceinline__ void scan_append(TkSmem& sm, const E* row, int64_t V,
     for (int u = 0; u < kUnroll; ++u) {
       if (it0 + u >= iters) break;  // the same for the whole CTA
       const int64_t v = (it0 + u) * kTkThreads + threadIdx.x;
-      const uint32_t w[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
-      uint32_t mask = 0;
       if (v < nvec) {
-#pragma unroll
-        for (int e = 0; e < kVec; ++e) {
-          uint32_t b;
-          if (sizeof(E) == 2) b = (e & 1) ? (w[e >> 1] & 0xffff0000u) : (w[e >> 1] << 16);
-          else b = w[e];
-          mask |= (key_of_bits(b) >= thr ? 1u : 0u) << e;
-        }
-      }
-      if (!__any_sync(kFull, mask != 0)) continue;
-      const uint32_t cnt = static_cast<uint32_t>(__popc(mask));
-      uint32_t incl = cnt;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(kFull, incl, o);
-        if (lane >= o) incl += y;
-      }
-      uint32_t base = 0;
-      if (lane == 31) base = atomicAdd(&sm.count, incl);
-      base = __shfl_sync(kFull, base, 31) + incl - cnt;
-      while (mask) {
-        const int e = __ffs(mask) - 1;
-        mask &= mask - 1;
-        const int c = sizeof(E) == 2 ? e >> 1 : e;  // the 32-bit word holding entry e (selects, no local array)
-        const uint32_t word = c == 0 ? q[u].x : c == 1 ? q[u].y : c == 2 ? q[u].z : q[u].w;
-        uint32_t b;
-        if (sizeof(E) == 2) b = (e & 1) ? (word & 0xffff0000u) : (word << 16);
-        else b = word;
-        if (base < static_cast<uint32_t>(kCap)) sm.cand[base] = composite(key_of_bits(b), v * kVec + e);
-        ++base;
+        const uint32_t mask = vec_hits<E>(q[u], thr);
+        if (mask) append_vec<E>(sm, q[u], mask, v * kVec);
       }
     }
   }

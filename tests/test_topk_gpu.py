@@ -2,8 +2,11 @@
 order (value descending, id ascending) makes the answer unique, so ids and values must
 match exactly.  The cases reach every path of the kernel: rows short enough to keep
 whole, the sampled threshold on long rows, the exact radix-select path (forced by heavy
-ties and by rows whose entries are all equal), rows that start off a 16-byte boundary,
-K = 1 and K = V, signed zeros and infinities."""
+ties and by rows whose entries are all equal), rows that start off a 16-byte boundary
+(entries before the first and after the last aligned 16-byte block are read apart from
+the bulk-copied body), rows with no aligned block at all, bodies that end inside a copy
+chunk and rows long enough to reuse every ring slot many times, K = 1 and K = V, signed
+zeros and infinities."""
 
 import numpy as np
 import pytest
@@ -75,6 +78,16 @@ def test_unaligned_rows_and_k_equals_v(dtype):
     run(bf16_grid(x) if dtype == "bf16" else x, 33, dtype)
     y = rng.standard_normal((4, 37)).astype(np.float32)
     run(bf16_grid(y) if dtype == "bf16" else y, 37, dtype)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("V", [1, 3, 5, 8, 9, 15, 16, 17, 31, 4097, 8191, 16385])
+def test_short_rows_every_alignment(dtype, V):
+    # 9 rows of V entries: row starts fall on every 2- (bf16) or 4-byte (f32) offset, so rows
+    # with no 16-byte block, with only a head and tail, and with a body ending mid-chunk occur
+    rng = np.random.default_rng(V)
+    x = rng.standard_normal((9, V)).astype(np.float32)
+    run(bf16_grid(x) if dtype == "bf16" else x, min(V, 3), dtype)
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
