@@ -178,8 +178,10 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// The same between the generic and the async proxy for global memory: written by plain
-// stores in one kernel role and read by TMA in another.
+// The same between the generic and the async proxy for global memory: orders a role's
+// global accesses against TMA traffic around the release or acquire of a completion
+// counter (the gradient buffers of a chunk backward, written by TMA stores in one CTA and
+// read by TMA loads in others).
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
