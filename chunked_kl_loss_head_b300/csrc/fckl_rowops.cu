@@ -177,20 +177,44 @@ __global__ void f32_to_bf16_kernel(const float4* __restrict__ src, __nv_bfloat16
   }
 }
 
-// Tiled transpose of a bf16 matrix through shared memory (32 x 32 tiles, coalesced on
-// both sides).
+// out[c, r] = in[r, c] for a [rows, cols] bf16 matrix: 64 x 64 tiles through shared memory
+// (rows 66 elements apart, so both the row-wise writes and the column-wise reads spread
+// over the banks), 16-byte global loads and stores wherever a tile row is whole and the
+// leading dimension and base allow it, element-wise at the edges.
 __global__ void transpose_bf16_kernel(const uint16_t* __restrict__ in, int64_t rows, int64_t cols, int64_t ld_in,
                                       uint16_t* __restrict__ out, int64_t ld_out) {
-  __shared__ uint16_t tile[32][33];
-  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * 32, r0 = static_cast<int64_t>(blockIdx.y) * 32;
-  for (int j = threadIdx.y; j < 32; j += 8) {
-    const int64_t r = r0 + j, c = c0 + threadIdx.x;
-    if (r < rows && c < cols) tile[j][threadIdx.x] = in[r * ld_in + c];
+  __shared__ __align__(16) uint16_t tile[64][66];
+  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * 64, c0 = static_cast<int64_t>(blockIdx.y) * 64;
+  const bool vin = ld_in % 8 == 0 && reinterpret_cast<uintptr_t>(in) % 16 == 0;
+  const bool vout = ld_out % 8 == 0 && reinterpret_cast<uintptr_t>(out) % 16 == 0;
+  for (int i = threadIdx.x; i < 512; i += blockDim.x) {
+    const int r = i >> 3, v = i & 7;
+    const int64_t gr = r0 + r, gc = c0 + v * 8;
+    uint32_t* t = reinterpret_cast<uint32_t*>(&tile[r][v * 8]);
+    if (gr < rows && vin && gc + 8 <= cols) {
+      const uint4 q = *reinterpret_cast<const uint4*>(in + gr * ld_in + gc);
+      t[0] = q.x;
+      t[1] = q.y;
+      t[2] = q.z;
+      t[3] = q.w;
+    } else {
+      for (int e = 0; e < 8; ++e) tile[r][v * 8 + e] = (gr < rows && gc + e < cols) ? in[gr * ld_in + gc + e] : 0;
+    }
   }
   __syncthreads();
-  for (int j = threadIdx.y; j < 32; j += 8) {
-    const int64_t c = c0 + j, r = r0 + threadIdx.x;
-    if (r < rows && c < cols) out[c * ld_out + r] = tile[threadIdx.x][j];
+  for (int i = threadIdx.x; i < 512; i += blockDim.x) {
+    const int oc = i >> 3, v = i & 7;  // output row c0 + oc, output columns r0 + 8v .. r0 + 8v + 7
+    const int64_t orow = c0 + oc, ocol = r0 + v * 8;
+    if (orow >= cols) continue;
+    uint32_t w[4];
+    for (int e = 0; e < 4; ++e)
+      w[e] = static_cast<uint32_t>(tile[v * 8 + 2 * e][oc]) | (static_cast<uint32_t>(tile[v * 8 + 2 * e + 1][oc]) << 16);
+    if (vout && ocol + 8 <= rows) {
+      *reinterpret_cast<uint4*>(out + orow * ld_out + ocol) = make_uint4(w[0], w[1], w[2], w[3]);
+    } else {
+      for (int e = 0; e < 8; ++e)
+        if (ocol + e < rows) out[orow * ld_out + ocol + e] = tile[v * 8 + e][oc];
+    }
   }
 }
 
@@ -198,9 +222,12 @@ __global__ void transpose_bf16_kernel(const uint16_t* __restrict__ in, int64_t r
 
 cudaError_t launch_transpose_bf16(const void* in, int64_t rows, int64_t cols, int64_t ld_in, void* out, int64_t ld_out,
                                   cudaStream_t st) {
-  const dim3 grid(static_cast<unsigned>((cols + 31) / 32), static_cast<unsigned>((rows + 31) / 32));
-  transpose_bf16_kernel<<<grid, dim3(32, 8), 0, st>>>(static_cast<const uint16_t*>(in), rows, cols, ld_in,
-                                                      static_cast<uint16_t*>(out), ld_out);
+  if (rows == 0 || cols == 0) return cudaSuccess;
+  // rows (the vocabulary when W is transposed) on grid x, whose limit is 2^31 - 1
+  if ((cols + 63) / 64 > 65535) return cudaErrorInvalidValue;
+  const dim3 grid(static_cast<unsigned>((rows + 63) / 64), static_cast<unsigned>((cols + 63) / 64));
+  transpose_bf16_kernel<<<grid, 256, 0, st>>>(static_cast<const uint16_t*>(in), rows, cols, ld_in,
+                                              static_cast<uint16_t*>(out), ld_out);
   return cudaGetLastError();
 }
 
