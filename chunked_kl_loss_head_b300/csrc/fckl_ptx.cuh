@@ -57,19 +57,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Waits for the phase with the given parity to complete; false after FCKL_WAIT_NS.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_ns();
-  for (uint32_t i = 0;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63) == 63) {
-      if (global_ns() - t0 > FCKL_WAIT_NS) return false;
-      __nanosleep(64);
-    }
-  }
-}
-
 // ---------------------------------------------------------------------------- clusters
 // The CTA-pair engine runs as clusters of two CTAs (ranks 0 and 1, on the two SMs of one
 // TPC); the helpers below address the peer CTA's shared memory.
@@ -191,11 +178,6 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const unsigned int* p) {
   uint32_t v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
-}
-
-// Named barrier `id` over `nthreads` threads (whole warps) of this CTA.
-__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 // ---------------------------------------------------------------------------- tcgen05
