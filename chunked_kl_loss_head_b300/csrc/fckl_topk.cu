@@ -11,8 +11,8 @@
 // a few times K row entries are expected above it: the filter threshold; the streaming
 // pass appends every entry at or above it to a shared-memory candidate list (a 16-byte
 // vector is ruled out by one signed max of its raw bits; a thread whose vector has
-// candidates takes one shared atomic for them), and a bitonic sort of the candidates,
-// first narrowed to about K, by (key, id) gives the answer.  When the sample misleads (fewer than K
+// candidates takes one shared atomic for them); the candidates, narrowed to about K, are
+// then put in (key, id) order by rank counting (or a bitonic sort for long lists).  When the sample misleads (fewer than K
 // candidates, or more than the list holds: heavy ties, tiny or adversarial rows) the row
 // takes the exact path: a 4-pass radix select of the K-th largest key, then every entry
 // above it plus the entries equal to it in id order.
@@ -455,7 +455,23 @@ __global__ void __launch_bounds__(kTkThreads) topk_kernel(const E* __restrict__ 
     }
   }
 
-  // ---- sort (padded with zeros, which sort last) and write the first K
+  // ---- order the candidates and write the first K.  With at most one candidate per
+  // thread, each thread counts the candidates ahead of its own (all distinct: the id is
+  // part of the composite) and writes it at that rank, with no barrier; longer lists are
+  // bitonic-sorted (padded with zeros, which sort last).
+  if (n <= static_cast<uint32_t>(kTkThreads)) {
+    if (static_cast<uint32_t>(tid) < n) {
+      const unsigned long long c = srt[tid];
+      uint32_t rank = 0;
+#pragma unroll 4
+      for (uint32_t j = 0; j < n; ++j) rank += srt[j] > c ? 1u : 0u;
+      if (rank < static_cast<uint32_t>(K)) {
+        out_idx[t * K + rank] = static_cast<int32_t>(0xffffffffu - static_cast<uint32_t>(c & 0xffffffffull));
+        out_val[t * K + rank] = __uint_as_float(bits_of_key(static_cast<uint32_t>(c >> 32)));
+      }
+    }
+    return;
+  }
   int np2 = 1;
   while (np2 < static_cast<int>(n)) np2 <<= 1;
   for (int i = static_cast<int>(n) + tid; i < np2; i += kTkThreads) srt[i] = 0ull;
