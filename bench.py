@@ -331,12 +331,24 @@ def run_topk(args, cfg):
         secs = time.perf_counter() - t0
         cpu = dict(value=rows / secs, unit="rows/s", cores=len(os.sched_getaffinity(0)), kind="oracle",
                    sample=f"oracle top-K (numpy lexsort per row) on rows 0..{rows - 1}; {secs:.2f} s")
+    # DRAM bytes per launch from the committed ncu capture of this workload, while the kernel
+    # source is the one that capture ran
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        try:
+            tj = json.load(open(tpath)).get("topk_bf16", {})
+            if tj.get("rows") == T and tj.get("V") == V and tj.get("K") == K and \
+                    tj.get("src_sha") == _src_sha(("fckl_topk.cu",)):
+                traffic = tj["bytes_per_launch"]
+        except (ValueError, KeyError):
+            traffic = None
     line = dict(metric="teacher top-K extraction rows/s", value=T / (ms / 1e3), unit="rows/s", n_gpus=1,
                 steps=args.steps, warmup=args.warmup, ms_per_step=ms, higher_is_better=True, scaling="weak",
                 vs_baseline=None, dtype="bf16", data="synthetic",
                 config=dict(workload=f"teacher logits [T={T}, V={V}] bf16, K={K}",
                             l2=f"input larger than L2 ({T * V * 2 / 1e9:.2f} GB)"),
-                roofline=dict(bound="hbm", achieved=gbs, peak=hbm, unit="GB/s", frac=gbs / hbm, traffic=None,
+                roofline=dict(bound="hbm", achieved=gbs, peak=hbm, unit="GB/s", frac=gbs / hbm, traffic=traffic,
                               peak_note=f"HBM copy ({peaks['source']})"),
                 cpu_baseline=cpu, gpu_launches=int(launches), clocks=clk.summary())
     print(json.dumps(line), flush=True)
@@ -585,10 +597,14 @@ def main():
 
 
 def _kernel_src_sha():
+    return _src_sha(("fckl_tc.cu", "fckl_ptx.cuh", "fckl_api.cu"))
+
+
+def _src_sha(files):
     import hashlib
 
     h = hashlib.sha256()
-    for f in ("fckl_tc.cu", "fckl_ptx.cuh", "fckl_api.cu"):
+    for f in files:
         h.update(open(os.path.join(ROOT, "chunked_kl_loss_head_b300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
