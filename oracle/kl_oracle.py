@@ -38,7 +38,7 @@ from __future__ import annotations
 
 import numpy as np
 
-__all__ = ["teacher_log_probs", "student_lse", "fwd_bwd", "dense_teacher"]
+__all__ = ["teacher_log_probs", "student_lse", "fwd_bwd"]
 
 
 def teacher_log_probs(topk_logits, tau):
@@ -53,16 +53,6 @@ def student_lse(s):
     """Row-wise logsumexp of the tempered student logits s[n, V]."""
     m = s.max(axis=1, keepdims=True)
     return (m + np.log(np.exp(s - m).sum(axis=1, keepdims=True)))[:, 0]
-
-
-def dense_teacher(topk_idx, topk_logits, tau, V):
-    """The dense teacher distribution p[n, V] (zero outside the cached ids)."""
-    logp = teacher_log_probs(topk_logits, tau)
-    n, K = logp.shape
-    P = np.zeros((n, V), dtype=np.float64)
-    rows = np.repeat(np.arange(n), K)
-    np.add.at(P, (rows, np.asarray(topk_idx, dtype=np.int64).ravel()), np.exp(logp).ravel())
-    return P
 
 
 def fwd_bwd(H, W, topk_idx, topk_logits, valid, tau, grad=1.0, N=None, want_grads=True,
