@@ -22,15 +22,24 @@ constexpr size_t kAlign = 256;
 // flight (one being written, two being read); the f32 path one.
 constexpr size_t kStripeBudgetBytes = size_t(96) << 20;
 constexpr size_t kStripeBudgetBytesF32 = size_t(64) << 20;
+// Rows of one backward block.  The backward works through a chunk in blocks of at most this
+// many rows, so a large chunk does not force narrow vocab stripes on it: with the stripe
+// budget above, blocks of 4096 rows get stripes of 4096 columns, the balance between the
+// per-stripe reduce of the block's dH accumulator and the per-block read-modify-write of
+// dW.  Smaller chunks keep their own size (and their smaller workspace).
+constexpr int64_t kBwdRowBlock = 4096;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct Sizes {
-  int64_t T, d, V, K, C, S, nvt, stripes;
+  int64_t T, d, V, K;
+  int64_t C;   // rows per chunk: one forward launch, and the per-chunk teacher scratch
+  int64_t Cb;  // rows per backward block: min(C, kBwdRowBlock)
+  int64_t S, nvt, stripes;
   size_t elem;  // bytes of one H / W / dH element
 };
 
-// The stripe width S of the backward (a multiple of 256 vocab columns).
+// The stripe width S of the backward for blocks of C rows (a multiple of 256 vocab columns).
 int64_t stripe_width(int64_t C, int64_t V, size_t elem) {
   const int64_t vpad = (V + kTileV - 1) / kTileV * kTileV;
   const size_t per_col = elem == 2 ? static_cast<size_t>(C) * 2 * static_cast<size_t>(tc_grad_buffers())
@@ -63,44 +72,30 @@ Layout layout_of(const Sizes& z) {
   L.slogp = take(4 * ck);
   L.zk = take(4 * ck);
   L.part = take(8 * static_cast<size_t>(z.C) * static_cast<size_t>(z.nvt));
-  L.G = take(static_cast<size_t>(z.C) * static_cast<size_t>(z.S) *
+  // backward block scratch: sized by the block, not the chunk
+  L.G = take(static_cast<size_t>(z.Cb) * static_cast<size_t>(z.S) *
              (z.elem == 2 ? 2 * static_cast<size_t>(tc_grad_buffers()) : 4));
   L.done = take(z.elem == 2 ? 2 * sizeof(unsigned int) * static_cast<size_t>(z.stripes) : 0);
-  L.dHacc = take(z.elem == 2 ? 4 * static_cast<size_t>(z.C) * static_cast<size_t>(z.d) : 0);
-  L.ldT = (z.C + 7) / 8 * 8;
+  L.dHacc = take(z.elem == 2 ? 4 * static_cast<size_t>(z.Cb) * static_cast<size_t>(z.d) : 0);
+  L.ldT = (z.Cb + 7) / 8 * 8;
   L.HcT = take(z.elem == 2 ? 2 * static_cast<size_t>(z.d) * static_cast<size_t>(L.ldT) : 0);
   L.total = off;
   return L;
 }
 
 bool sizes_of(int64_t T, int64_t d, int64_t V, int32_t K, int64_t chunk, fckl_dtype dt, Sizes* z) {
-  if (T < 0 || d < 1 || V < 1 || K < 1 || K > FCKL_MAX_K || chunk < 1) return false;
-  if (dt != FCKL_F32 && dt != FCKL_BF16) return false;
-  if (V >= (int64_t(1) << 31) || T >= (int64_t(1) << 31) || d >= (int64_t(1) << 31)) return false;
+  if (!valid_sizes(T, d, V, K, chunk, dt)) return false;
   z->T = T;
   z->d = d;
   z->V = V;
   z->K = K;
   z->C = T == 0 ? 1 : (chunk < T ? chunk : T);
+  z->Cb = z->C < kBwdRowBlock ? z->C : kBwdRowBlock;
   z->elem = dt == FCKL_BF16 ? 2 : 4;
-  z->S = stripe_width(z->C, V, z->elem);
+  z->S = stripe_width(z->Cb, V, z->elem);
   z->stripes = (V + z->S - 1) / z->S;
   z->nvt = (V + kTileV - 1) / kTileV;
   return true;
-}
-
-bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-
-// Device check: the kernels are built for sm_103a only.
-fckl_status device_info(int* num_sms) {
-  int dev = 0, major = 0, minor = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return FCKL_ERR_CUDA;
-  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return FCKL_ERR_CUDA;
-  if (major != 10 || minor != 3) return FCKL_ERR_UNSUPPORTED;
-  return FCKL_OK;
 }
 
 // Checks shared by forward and backward.
@@ -161,25 +156,26 @@ cudaEvent_t pool_get() {
   return e;
 }
 
-// Runs one launch step: counts it, brackets it with events when profiling is on, and
-// maps a CUDA error to FCKL_ERR_CUDA.
-template <class F>
-fckl_status step(fckl_kernel_class cls, cudaStream_t st, F&& launch) {
-  prof_begin(cls, st);
-  const cudaError_t e = launch();
-  prof_end(cls, st);
-  if (e != cudaSuccess) return FCKL_ERR_CUDA;
-  count_launch(cls);
-  return FCKL_OK;
+}  // namespace
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool valid_sizes(int64_t T, int64_t d, int64_t V, int32_t K, int64_t chunk, fckl_dtype dt) {
+  if (T < 0 || d < 1 || V < 1 || K < 1 || K > FCKL_MAX_K || chunk < 1) return false;
+  if (dt != FCKL_F32 && dt != FCKL_BF16) return false;
+  return V < (int64_t(1) << 31) && T < (int64_t(1) << 31) && d < (int64_t(1) << 31);
 }
 
-#define FCKL_TRY(expr)                 \
-  do {                                 \
-    const fckl_status _s = (expr);     \
-    if (_s != FCKL_OK) return _s;      \
-  } while (0)
-
-}  // namespace
+fckl_status device_info(int* num_sms) {
+  int dev = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FCKL_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return FCKL_ERR_CUDA;
+  if (major != 10 || minor != 3) return FCKL_ERR_UNSUPPORTED;
+  return FCKL_OK;
+}
 
 void count_launch(fckl_kernel_class) { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
@@ -318,8 +314,8 @@ fckl_status fckl_backward(const void* H, const void* W, const int32_t* topk_idx,
   TileSched sched{&ctrl->tile_counter, 0};
   FCKL_TRY(step(FCKL_K_REDUCE, st, [&] { return launch_grad_scale(valid, T, tau, grad_loss, grad_scale, ctrl, st); }));
   const int64_t S = z.S;
-  for (int64_t c0 = 0; c0 < T; c0 += z.C) {
-    const int64_t rows = (T - c0 < z.C) ? T - c0 : z.C;
+  for (int64_t c0 = 0; c0 < T; c0 += z.Cb) {
+    const int64_t rows = (T - c0 < z.Cb) ? T - c0 : z.Cb;
     FCKL_TRY(step(FCKL_K_PREP, st, [&] {
       return launch_prep(topk_idx + c0 * K, topk_logits + c0 * K, rows, K, V, tau, s, ctrl, st);
     }));
@@ -375,6 +371,27 @@ fckl_status fckl_topk_extract(const void* logits, int64_t T, int64_t V, int32_t 
   FCKL_TRY(device_info(&num_sms));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   return step(FCKL_K_TOPK, st, [&] { return launch_topk(logits, T, V, K, dtype, topk_idx, topk_logits, st); });
+}
+
+fckl_status fckl_loss_partials(const void* ws, size_t ws_bytes, double* partials, void* stream) {
+  if (!ws || !aligned(ws, kAlign) || ws_bytes < kCtrlBytes) return FCKL_ERR_WORKSPACE;
+  if (!partials || !aligned(partials, 8)) return FCKL_ERR_INVALID_ARG;
+  int num_sms = 0;
+  FCKL_TRY(device_info(&num_sms));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const Ctrl* ctrl = static_cast<const Ctrl*>(ws);
+  return step(FCKL_K_REDUCE, st, [&] { return launch_loss_partials(ctrl, partials, st); });
+}
+
+fckl_status fckl_loss_finish(const double* total, const double* local, float* loss, float* grad_scale,
+                             void* stream) {
+  if (!total || !local || !loss || !grad_scale) return FCKL_ERR_INVALID_ARG;
+  if (!aligned(total, 8) || !aligned(local, 8) || !aligned(loss, 4) || !aligned(grad_scale, 4))
+    return FCKL_ERR_INVALID_ARG;
+  int num_sms = 0;
+  FCKL_TRY(device_info(&num_sms));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return step(FCKL_K_REDUCE, st, [&] { return launch_loss_finish(total, local, loss, grad_scale, st); });
 }
 
 fckl_status fckl_get_error(void* ws, void* stream) {

@@ -62,6 +62,9 @@ cudaError_t launch_loss_reduce(const float* row_loss, const uint8_t* valid, int6
                                Ctrl* ctrl, cudaStream_t st);
 cudaError_t launch_grad_scale(const uint8_t* valid, int64_t T, float tau, float grad_loss,
                               const float* grad_scale, Ctrl* ctrl, cudaStream_t st);
+cudaError_t launch_loss_partials(const Ctrl* ctrl, double* out, cudaStream_t st);
+cudaError_t launch_loss_finish(const double* total, const double* local, float* loss, float* grad_scale,
+                               cudaStream_t st);
 cudaError_t launch_f32_to_bf16(const float* src, void* dst, int64_t n, cudaStream_t st);
 // out[c, r] = in[r, c] for bf16 in[rows, cols] (row stride ld_in) -> out[cols, ld_out]
 cudaError_t launch_transpose_bf16(const void* in, int64_t rows, int64_t cols, int64_t ld_in, void* out,
@@ -107,6 +110,13 @@ cudaError_t tc_debug_gemm(const void* A, const void* B, float* D, int64_t M, int
                           int a_mn, int b_mn, int cta_pair, int num_sms, cudaStream_t st);
 
 // ---- host helpers (fckl_api.cu) ----------------------------------------------------------
+// Size arguments every loss entry point shares: T >= 0, d, V >= 1, 1 <= K <= FCKL_MAX_K,
+// chunk >= 1, a known dtype, and T, d, V below 2^31.
+bool valid_sizes(int64_t T, int64_t d, int64_t V, int32_t K, int64_t chunk, fckl_dtype dt);
+// Device check (the kernels are built for sm_103a only) and the SM count of the current
+// device.
+fckl_status device_info(int* num_sms);
+bool aligned(const void* p, size_t a);
 bool encode_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                          uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer);
 bool encode_tmap_f32_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
@@ -114,5 +124,23 @@ bool encode_tmap_f32_2d(CUtensorMap* map, const void* base, uint64_t inner, uint
 void count_launch(fckl_kernel_class cls);
 void prof_begin(fckl_kernel_class cls, cudaStream_t st);
 void prof_end(fckl_kernel_class cls, cudaStream_t st);
+
+// Runs one launch step: counts it, brackets it with events when profiling is on, and maps a
+// CUDA error to FCKL_ERR_CUDA.
+template <class F>
+fckl_status step(fckl_kernel_class cls, cudaStream_t st, F&& launch) {
+  prof_begin(cls, st);
+  const cudaError_t e = launch();
+  prof_end(cls, st);
+  if (e != cudaSuccess) return FCKL_ERR_CUDA;
+  count_launch(cls);
+  return FCKL_OK;
+}
+
+#define FCKL_TRY(expr)             \
+  do {                             \
+    const fckl_status _s = (expr); \
+    if (_s != FCKL_OK) return _s;  \
+  } while (0)
 
 }  // namespace fckl

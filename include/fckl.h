@@ -100,6 +100,8 @@ FCKL_API fckl_status fckl_forward(const void* H, const void* W, const int32_t* t
 /* Backward: dH and dW of g * loss, recomputing the logit tiles chunk by chunk
  * (the extra projection work in the backward pass that chunking costs,
  * axbrief.com, "Breaking the Bottleneck with Offline Caching and Chunked Loss").
+ * A chunk is worked through in row blocks of at most 4096 rows (all of it when the chunk
+ * is smaller), each block over every vocab stripe; the chunk bounds the workspace.
  *   lse        device float32 [T] from fckl_forward with the same inputs
  *   grad_loss  host scalar g (dL/dloss)
  *   grad_scale device float32 scalar or NULL; when given, g is multiplied by it
@@ -129,6 +131,31 @@ FCKL_API fckl_status fckl_backward(const void* H, const void* W, const int32_t* 
  * `stream`; returns FCKL_OK once the work is queued. */
 FCKL_API fckl_status fckl_topk_extract(const void* logits, int64_t T, int64_t V, int32_t K, fckl_dtype dtype,
                                        int32_t* topk_idx, float* topk_logits, void* stream);
+
+/* ---- token-sharded data parallelism ---------------------------------------------------
+ * The pages place the method in distillation runs that would otherwise be spread over many
+ * GPUs and nodes (getaibook.com, "Hardware and Performance Tradeoffs"; axbrief.com,
+ * "Quantifying the Efficiency Gain: 15.6x VRAM Reduction").  The loss shards over tokens:
+ * each rank runs fckl_forward / fckl_backward on its own rows (H, topk_idx, topk_logits,
+ * valid) with the whole W.  Three things cross ranks: the loss sum and N, which the mean
+ * and the gradient scale g / (tau N) need over all ranks, and dW, which sums over ranks;
+ * dH stays with its rank.  These two calls hand the first two to the caller's collective
+ * (a sum over ranks, e.g. an all-reduce) and back; dW is summed by the caller as is.
+ *
+ * Writes partials (device double[2], 8-byte aligned) = { sum of loss_t over the valid rows,
+ * N } of the last fckl_forward on workspace `ws`, stream-ordered after it. */
+FCKL_API fckl_status fckl_loss_partials(const void* ws, size_t ws_bytes, double* partials, void* stream);
+
+/* From total (device double[2]: the partials summed over ranks) and this rank's own partials
+ * `local`, writes
+ *   loss       device float32 scalar: total[0] / total[1], the mean over all ranks' valid
+ *              rows (0 when total[1] == 0)
+ *   grad_scale device float32 scalar: local[1] / total[1] (0 when total[1] == 0); passed as
+ *              fckl_backward's grad_scale on this rank, it makes the gradient scale
+ *              g / (tau N_total), so that the ranks' dW add up to the whole batch's.
+ * Asynchronous on `stream`. */
+FCKL_API fckl_status fckl_loss_finish(const double* total, const double* local, float* loss, float* grad_scale,
+                                      void* stream);
 
 /* Waits for `stream`, then returns and clears the status word the GPU wrote in
  * the workspace (FCKL_OK, FCKL_ERR_BAD_INDEX or FCKL_ERR_TIMEOUT), or
@@ -207,8 +234,9 @@ FCKL_API fckl_status fckl_debug_gemm_bf16(const void* A, const void* B, float* D
  * (16*K + 8*ceil(V/256) bytes per row) would not fit; the results do not depend on the
  * chunk size.  Returns FCKL_ERR_WORKSPACE when a single row's scratch exceeds
  * FCKL_NOALLOC_SCRATCH_BYTES, before anything is launched.
- * The first call on a device looks up the array's device address (and may load the
- * library's GPU code); make that first call before any stream capture.  All calls share
+ * Every call looks up the array's device address on the current device; the first call on
+ * a device may also load the library's GPU code, so make that first call before any stream
+ * capture.  All calls share
  * the one array, which keeps the last call's contents: the call clears what must start at
  * zero itself, but calls that overlap on the GPU (other streams or host threads on the
  * same device) race on it and must be serialized by the caller. */

@@ -1,9 +1,12 @@
 """CUDA path vs the fp64 oracle at the full sizes of the four bf16 workloads, in the
 launch configuration the benchmark times (the workload's chunk size, the library's
-own vocab stripes).
+own backward row blocks and vocab stripes).
 
-At these sizes the oracle cannot build every logit row (the gpt-oss-shaped workload
-alone is 1.5e14 fp64 multiply-adds per pass), so the checks are:
+The Llama-shaped workload (8192 rows) is checked whole: loss, lse, per-row losses,
+every dH row and every dW row against the oracle's full-vocabulary rows.
+
+The larger workloads are too big for the oracle to build every logit row (the
+gpt-oss-shaped one alone is 1.5e14 fp64 multiply-adds per pass), so for them:
 
 * sampled rows: lse_t, loss_t and the dH row of ~60 rows (valid rows spread over
   every chunk, the chunk edges and the ragged tail, plus ignored rows) against the
@@ -12,8 +15,12 @@ alone is 1.5e14 fp64 multiply-adds per pass), so the checks are:
   valid rows (each of which is tied to the oracle by the sampled rows).
 * ignored rows: dH rows exactly zero, loss_t exactly zero, on every row.
 * dW, three ways, since no dW row is independent of the other tokens:
-  - a token prefix of the same workload (same d, V, K, tau, generators) against the
-    oracle's whole dW;
+  - a 4096-token prefix of the same workload (same d, V, K, tau, generators) at the
+    benchmark's chunk, so the same backward blocks and vocab stripes (all gradient
+    buffers rotating, the ragged last stripe, d's narrow last tile): every dH row,
+    and the dW rows at every stripe and tile edge, in the ragged last stripe up to
+    V - 1, the most frequent teacher ids and rows no teacher id hits, against the
+    oracle;
   - additivity: dW of all T rows = dW of rows [0, t1) + dW of rows [t1, T), each
     part scaled to the global N (the data-parallel identity of the loss);
   - every valid row of dz sums to zero over the vocabulary (sum q = sum p = 1), so
@@ -34,7 +41,8 @@ pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
 N_SAMPLE_VALID = 48
 N_SAMPLE_IGNORED = 8
-PREFIX_ROWS = 256
+PREFIX_ROWS = 4096
+ORACLE_ROW_BLOCK = 256  # rows per block of the oracle's logit rows (host memory only)
 
 
 def _dev(a):
@@ -104,7 +112,7 @@ class Workload:
         x = make_rows(self.cfg, rows)
         H = bf16_bits_to_f32(x["H"]).astype(np.float64)
         return fwd_bwd(H, self.W64, x["topk_idx"], x["topk_logits"], x["valid"], self.cfg.tau, N=self.N,
-                       dW_rows=None if want_dW else [])
+                       dW_rows=None if want_dW else [], row_block=ORACLE_ROW_BLOCK)
 
 
 _CACHE = {}
@@ -163,24 +171,100 @@ def check_dW_column_sums(wl, got):
     assert ratio <= 6.0
 
 
-def check_prefix_dW(wl, chunk):
-    rows = np.arange(PREFIX_ROWS)
-    sub = wl.run(min(chunk, 128), rows=slice(0, PREFIX_ROWS), grad_loss=1.0)
-    assert sub["status"] == 0
+def _worst(err_rows, ids, n=5):
+    """The n largest per-row errors as 'id:err' text, for failure messages."""
+    order = np.argsort(-err_rows)[:n]
+    return ", ".join(f"{int(ids[i])}:{err_rows[i]:.2e}" for i in order)
+
+
+def _row_errors(got, ref):
+    """Per-row max |got - ref|, over max |ref| of the whole tensor."""
+    den = max(float(np.abs(ref).max(initial=0.0)), 1e-300)
+    return np.abs(np.asarray(got, np.float64) - ref).max(axis=1) / den
+
+
+def dW_check_rows(V, prefix_idx, seed=99):
+    """Vocab rows of dW checked on a prefix: both sides of every multiple of 256 up to
+    1024 and of every multiple of 1024 (every tile edge of the first stripe and every
+    stripe edge, whatever the stripe width, a multiple of 1024 here), the last 512 rows
+    (the ragged last stripe, up to V - 1), the 256 most frequent teacher ids, 64 rows no
+    teacher id of the prefix hits, and 256 random rows."""
+    rng = np.random.default_rng(seed)
+    edges = [e for m in list(range(256, 1025, 256)) + list(range(1024, V, 1024)) for e in (m - 1, m)]
+    hits = np.bincount(np.asarray(prefix_idx).ravel(), minlength=V)
+    frequent = np.argsort(-hits, kind="stable")[:256]
+    unhit = np.nonzero(hits == 0)[0]
+    none = rng.choice(unhit, min(64, len(unhit)), replace=False) if len(unhit) else []
+    rows = np.concatenate([np.asarray(edges, np.int64), np.arange(max(0, V - 512), V), frequent, none,
+                           rng.choice(V, 256, replace=False)])
+    return np.unique(rows[(rows >= 0) & (rows < V)])
+
+
+def check_prefix(wl, chunk, prefix_rows=PREFIX_ROWS):
+    """A token prefix of the workload at `chunk`: loss, every lse / loss_t / dH row and the
+    dW rows of dW_check_rows against the oracle (which builds every logit row)."""
+    rows = np.arange(prefix_rows)
+    sub = wl.run(chunk, rows=slice(0, prefix_rows), grad_loss=1.0)
+    assert sub["status"] == 0, api.fckl_status_string(sub["status"])
     from oracle import fwd_bwd
 
     x = make_rows(wl.cfg, rows)
     H = bf16_bits_to_f32(x["H"]).astype(np.float64)
-    ref = fwd_bwd(H, wl.W64, x["topk_idx"], x["topk_logits"], x["valid"], wl.cfg.tau)
-    e_dW = rel_max(sub["dW"].cpu().numpy(), ref["dW"])
-    e_dH = rel_max(sub["dH"].float().cpu().numpy(), ref["dH"])
+    vrows = dW_check_rows(wl.cfg.V, x["topk_idx"])
+    ref = fwd_bwd(H, wl.W64, x["topk_idx"], x["topk_logits"], x["valid"], wl.cfg.tau, dW_rows=vrows,
+                  row_block=ORACLE_ROW_BLOCK)
+    tol = TOL["bf16"]
     e_loss = rel(sub["loss"].item(), ref["loss"])
-    print(f"{wl.cfg.name}: prefix of {PREFIX_ROWS} rows: loss {e_loss:.2e} dH {e_dH:.2e} dW {e_dW:.2e}")
-    assert e_loss <= TOL["bf16"]["loss"]
-    assert e_dH <= TOL["bf16"]["grad"] and e_dW <= TOL["bf16"]["grad"]
+    e_lse = rel_max(sub["lse"].cpu().numpy(), ref["lse"])
+    dH = sub["dH"].float().cpu().numpy()
+    dW = sub["dW"][torch.from_numpy(vrows).cuda()].cpu().numpy()
+    rows_dH, rows_dW = _row_errors(dH, ref["dH"]), _row_errors(dW, ref["dW"])
+    msg = (f"{wl.cfg.name} chunk={chunk}: prefix of {prefix_rows} rows: loss {e_loss:.2e} lse {e_lse:.2e} "
+           f"dH {rows_dH.max():.2e} (worst rows {_worst(rows_dH, rows)}) "
+           f"dW {rows_dW.max():.2e} over {len(vrows)} vocab rows (worst {_worst(rows_dW, vrows)})")
+    print(msg)
+    assert e_loss <= tol["loss"] and e_lse <= tol["loss"], msg
+    assert rows_dH.max() <= tol["grad"] and rows_dW.max() <= tol["grad"], msg
+    assert np.all(dH[~x["valid"].astype(bool)] == 0.0), msg
 
 
-@pytest.mark.parametrize("name", ["llama_bf16", "stress_bf16", "gptoss_bf16"])
+def check_all_rows(wl, got):
+    """Every output of a whole workload against the oracle (feasible at 8192 rows)."""
+    from oracle import fwd_bwd
+
+    x = make_rows(wl.cfg, np.arange(wl.cfg.T))
+    H = bf16_bits_to_f32(x["H"]).astype(np.float64)
+    ref = fwd_bwd(H, wl.W64, x["topk_idx"], x["topk_logits"], x["valid"], wl.cfg.tau, row_block=ORACLE_ROW_BLOCK)
+    del H
+    tol = TOL["bf16"]
+    rows = np.arange(wl.cfg.T)
+    e_loss = rel(got["loss"].item(), ref["loss"])
+    e_lse = rel_max(got["lse"].cpu().numpy(), ref["lse"])
+    rl = got["row_loss"].cpu().numpy()
+    e_rl = rel_max(rl, ref["row_loss"])
+    rows_dH = _row_errors(got["dH"].float().cpu().numpy(), ref.pop("dH"))
+    rows_dW = _row_errors(got["dW"].cpu().numpy(), ref.pop("dW"))
+    msg = (f"{wl.cfg.name}: all {wl.cfg.T} rows: loss {e_loss:.2e} lse {e_lse:.2e} loss_t {e_rl:.2e} "
+           f"dH {rows_dH.max():.2e} (worst rows {_worst(rows_dH, rows)}) "
+           f"dW {rows_dW.max():.2e} (worst vocab rows {_worst(rows_dW, np.arange(wl.cfg.V))})")
+    print(msg)
+    assert e_loss <= tol["loss"] and e_lse <= tol["loss"] and e_rl <= tol["loss"], msg
+    assert rows_dH.max() <= tol["grad"] and rows_dW.max() <= tol["grad"], msg
+
+
+def test_llama_workload_all_rows():
+    """The Llama-shaped workload (8192 rows, two chunks of 4096, d = 3072, V = 128256) against
+    the oracle on every row and every dW row."""
+    wl = workload("llama_bf16")
+    chunk = wl.cfg.chunks[0]
+    got = wl.run(chunk)
+    assert got["status"] == 0, api.fckl_status_string(got["status"])
+    check_mean_and_ignored(wl, got)
+    check_dW_column_sums(wl, got)
+    check_all_rows(wl, got)
+
+
+@pytest.mark.parametrize("name", ["stress_bf16", "gptoss_bf16"])
 def test_full_size_workload(name):
     wl = workload(name)
     chunk = wl.cfg.chunks[0]
@@ -190,7 +274,7 @@ def test_full_size_workload(name):
     check_sampled_rows(wl, got, chunk)
     check_dW_column_sums(wl, got)
     del got
-    check_prefix_dW(wl, chunk)
+    check_prefix(wl, chunk)
 
 
 def test_full_size_dW_additivity():
@@ -224,6 +308,8 @@ def test_long_context_chunk_sweep():
             check_mean_and_ignored(wl, got)
             check_sampled_rows(wl, got, chunk)
             check_dW_column_sums(wl, got)
+        if chunk == 16384:
+            check_sampled_rows(wl, got, chunk)
         runs[chunk] = dict(loss=got["loss"].item(), lse=got["lse"].cpu(), row_loss=got["row_loss"].cpu(),
                            dW=got["dW"], dH=got["dH"])
         del got
@@ -235,4 +321,10 @@ def test_long_context_chunk_sweep():
         e_dH = float(((r["dH"].float() - base["dH"].float()).abs().max() / base["dH"].float().abs().max()).item())
         print(f"chunk {chunk} vs 4096: dW {e_dW:.2e} dH {e_dH:.2e}")
         assert e_dW <= 1e-3 and e_dH <= 1e-2
-    check_prefix_dW(wl, 1024)
+        if chunk == 16384:
+            # chunks above 4096 rows run their backward in 4096-row blocks: the same
+            # gradient arithmetic as chunks of 4096
+            assert torch.equal(r["dW"], base["dW"]) and torch.equal(r["dH"], base["dH"])
+    del runs, base
+    # chunk 1024: four chunks of the prefix, 16384-column stripes (13, the last ragged)
+    check_prefix(wl, 1024)

@@ -82,9 +82,24 @@ def test_fp32_several_chunks_and_stripes():
 
 
 def test_bf16_several_chunks_and_stripes():
-    # chunk 4096 -> stripes of 8192 vocab columns: 3 stripes, the last ragged (3616 columns)
+    # chunk 4096 -> stripes of 4096 vocab columns: 5 stripes, the last ragged (3616 columns),
+    # so all three gradient buffers rotate
     x = make_small(T=5000, d=64, V=20000, K=13, tau=1.5, dtype="bf16", seed=1, mask="random", mask_frac=0.1)
     check(x, run_gpu(x, 4096), label="bf16 multi-chunk/stripe")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_chunk_above_the_backward_block(dtype):
+    # chunk 6000: forward chunks of 6000 + 3000 rows, backward blocks of 4096 + 4096 + 808
+    x = make_small(T=9000, d=64, V=20000, K=11, tau=1.2, dtype=dtype, seed=15, mask="random", mask_frac=0.1)
+    a = run_gpu(x, 6000)
+    check(x, a, label=f"{dtype} chunk 6000")
+    b = run_gpu(x, 4096)
+    # the backward blocks are the same as chunk 4096's, so the gradients are bit for bit equal
+    assert a["loss"] == b["loss"]
+    np.testing.assert_array_equal(a["lse"], b["lse"])
+    np.testing.assert_array_equal(a["dW"], b["dW"])
+    np.testing.assert_array_equal(a["dH"], b["dH"])
 
 
 @pytest.mark.parametrize("chunk", [128, 100, 1000])
