@@ -4,7 +4,6 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
-#include <mutex>
 
 #include "fckl_internal.h"
 
@@ -15,23 +14,15 @@ namespace {
 // is loaded, on every GPU that loads it.
 static __device__ __align__(256) uint8_t g_noalloc_scratch[FCKL_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices];  // device address of g_noalloc_scratch, per device
-
 // Device address of the scratch array on the current device.  Host code cannot use the
 // symbol itself (on the host it names a stand-in, not device memory), so the address is
-// looked up once per device with that device current and kept.
+// looked up with that device current, on every call: the lookup is cheap once the
+// library's GPU code is loaded, and an address kept from an earlier call would go stale
+// if the device's context were torn down and the code loaded again elsewhere.
 fckl_status scratch_address(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FCKL_ERR_CUDA;
-  std::lock_guard<std::mutex> g(g_mu);
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return FCKL_ERR_CUDA;
-    g_scratch_addr[dev] = p;
-  }
-  *out = g_scratch_addr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return FCKL_ERR_CUDA;
+  *out = p;
   return FCKL_OK;
 }
 
@@ -42,8 +33,6 @@ size_t chunk_bytes(int64_t rows, int64_t K, int64_t nvt) {
   const size_t ck = static_cast<size_t>(rows) * static_cast<size_t>(K);
   return up256(sizeof(Ctrl)) + 4 * up256(4 * ck) + up256(8 * static_cast<size_t>(rows) * static_cast<size_t>(nvt));
 }
-
-bool is_aligned(const void* p, size_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
 
 }  // namespace
 }  // namespace fckl
@@ -56,15 +45,12 @@ extern "C" fckl_status fckl_forward_noalloc(const void* H, const void* W, const 
                                             float* loss, float* lse, float* row_loss, int32_t* status,
                                             void* stream) {
   // ---- argument checks (nothing is launched or looked up before they pass)
-  if (T < 0 || d < 1 || V < 1 || K < 1 || K > FCKL_MAX_K || chunk < 1) return FCKL_ERR_INVALID_ARG;
-  if (dtype != FCKL_F32 && dtype != FCKL_BF16) return FCKL_ERR_INVALID_ARG;
-  if (V >= (int64_t(1) << 31) || T >= (int64_t(1) << 31) || d >= (int64_t(1) << 31)) return FCKL_ERR_INVALID_ARG;
+  if (!valid_sizes(T, d, V, K, chunk, dtype)) return FCKL_ERR_INVALID_ARG;
   if (!(tau > 0.f) || !std::isfinite(tau)) return FCKL_ERR_INVALID_ARG;
   if (!loss) return FCKL_ERR_INVALID_ARG;
   if (T > 0 && (!H || !W || !topk_idx || !topk_logits || !valid || !lse || !row_loss)) return FCKL_ERR_INVALID_ARG;
-  if (!is_aligned(topk_idx, 4) || !is_aligned(topk_logits, 4)) return FCKL_ERR_UNSUPPORTED;
-  if (dtype == FCKL_BF16 ? (d % 8 != 0 || !is_aligned(H, 16) || !is_aligned(W, 16))
-                         : (!is_aligned(H, 4) || !is_aligned(W, 4)))
+  if (!aligned(topk_idx, 4) || !aligned(topk_logits, 4)) return FCKL_ERR_UNSUPPORTED;
+  if (dtype == FCKL_BF16 ? (d % 8 != 0 || !aligned(H, 16) || !aligned(W, 16)) : (!aligned(H, 4) || !aligned(W, 4)))
     return FCKL_ERR_UNSUPPORTED;
   const int64_t nvt = (V + kTileV - 1) / kTileV;
   // the largest chunk that fits the fixed scratch (a multiple of 128 rows when possible);
@@ -76,16 +62,10 @@ extern "C" fckl_status fckl_forward_noalloc(const void* H, const void* W, const 
   }
 
   // ---- device and scratch
-  int dev = 0, major = 0, minor = 0, num_sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return FCKL_ERR_CUDA;
-  if (major != 10 || minor != 3) return FCKL_ERR_UNSUPPORTED;
+  int num_sms = 0;
+  FCKL_TRY(device_info(&num_sms));
   void* base = nullptr;
-  const fckl_status sa = scratch_address(&base);
-  if (sa != FCKL_OK) return sa;
+  FCKL_TRY(scratch_address(&base));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
   uint8_t* b = static_cast<uint8_t*>(base);
@@ -103,33 +83,31 @@ extern "C" fckl_status fckl_forward_noalloc(const void* H, const void* W, const 
   off += up256(4 * ck);
   s.part = reinterpret_cast<float2*>(b + off);
 
-  // the previous call's status word must not leak into this one
-  if (cudaMemsetAsync(ctrl, 0, sizeof(Ctrl), st) != cudaSuccess) return FCKL_ERR_CUDA;
+  // the previous call's status word and tile counter must not leak into this one
+  FCKL_TRY(step(FCKL_K_OTHER, st, [&] { return cudaMemsetAsync(ctrl, 0, sizeof(Ctrl), st); }));
   TileSched sched{&ctrl->tile_counter, 0};
   const int nv = static_cast<int>(nvt);
   for (int64_t c0 = 0; c0 < T; c0 += rows_max) {
     const int64_t rows = (T - c0 < rows_max) ? T - c0 : rows_max;
-    if (launch_prep(topk_idx + c0 * K, topk_logits + c0 * K, rows, K, V, tau, s, ctrl, st) != cudaSuccess)
-      return FCKL_ERR_CUDA;
-    count_launch(FCKL_K_PREP);
-    cudaError_t e;
-    if (dtype == FCKL_BF16) {
-      e = tc_fwd_tiles(static_cast<const uint8_t*>(H) + c0 * d * 2, W, rows, d, V, tau, s.sidx, K, s.zk, s.part, nv,
-                       ctrl, &sched, num_sms, st);
-    } else {
-      e = launch_simt_fwd_tiles(static_cast<const float*>(H) + c0 * d, static_cast<const float*>(W), rows, d, V, tau,
-                                s.sidx, K, s.zk, s.part, nv, st);
-    }
-    if (e != cudaSuccess) return FCKL_ERR_CUDA;
-    count_launch(FCKL_K_FWD_TILES);
-    if (launch_combine(s.part, nv, s.zk, s.sp, s.slogp, valid + c0, rows, K, tau, lse + c0, row_loss + c0, st) !=
-        cudaSuccess)
-      return FCKL_ERR_CUDA;
-    count_launch(FCKL_K_COMBINE);
+    FCKL_TRY(step(FCKL_K_PREP, st, [&] {
+      return launch_prep(topk_idx + c0 * K, topk_logits + c0 * K, rows, K, V, tau, s, ctrl, st);
+    }));
+    FCKL_TRY(step(FCKL_K_FWD_TILES, st, [&] {
+      if (dtype == FCKL_BF16)
+        return tc_fwd_tiles(static_cast<const uint8_t*>(H) + c0 * d * 2, W, rows, d, V, tau, s.sidx, K, s.zk,
+                            s.part, nv, ctrl, &sched, num_sms, st);
+      return launch_simt_fwd_tiles(static_cast<const float*>(H) + c0 * d, static_cast<const float*>(W), rows, d, V,
+                                   tau, s.sidx, K, s.zk, s.part, nv, st);
+    }));
+    FCKL_TRY(step(FCKL_K_COMBINE, st, [&] {
+      return launch_combine(s.part, nv, s.zk, s.sp, s.slogp, valid + c0, rows, K, tau, lse + c0, row_loss + c0, st);
+    }));
   }
-  if (launch_loss_reduce(row_loss, valid, T, loss, ctrl, st) != cudaSuccess) return FCKL_ERR_CUDA;
-  count_launch(FCKL_K_REDUCE);
-  if (status && cudaMemcpyAsync(status, &ctrl->status, sizeof(int32_t), cudaMemcpyDeviceToDevice, st) != cudaSuccess)
-    return FCKL_ERR_CUDA;
+  FCKL_TRY(step(FCKL_K_REDUCE, st, [&] { return launch_loss_reduce(row_loss, valid, T, loss, ctrl, st); }));
+  if (status) {
+    FCKL_TRY(step(FCKL_K_OTHER, st, [&] {
+      return cudaMemcpyAsync(status, &ctrl->status, sizeof(int32_t), cudaMemcpyDeviceToDevice, st);
+    }));
+  }
   return FCKL_OK;
 }

@@ -1,5 +1,6 @@
 """Out-of-bounds writes, checked without a sanitizer: every buffer the library writes
-(the workspace, loss, lse, per-row losses, dH, dW, and the top-K outputs) is carved out of
+(the workspace, loss, lse, per-row losses, dH, dW, the top-K outputs, and the outputs of
+the allocation-free forward) is carved out of
 a larger allocation whose margins hold a known byte pattern; after the calls the margins
 must be untouched and the results must still match the oracle.  The shapes put ragged
 edges everywhere: rows not a multiple of the 256-row tile, a vocabulary not a multiple of
@@ -41,7 +42,8 @@ def _nbytes(dtype, shape):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
-@pytest.mark.parametrize("T,d,V,K,chunk", [(300, 64, 1000, 7, 128), (1000, 256, 50001, 20, 384)])
+@pytest.mark.parametrize("T,d,V,K,chunk", [(300, 64, 1000, 7, 128), (1000, 256, 50001, 20, 384),
+                                           (5000, 64, 9000, 5, 4500)])
 def test_loss_writes_stay_in_bounds(dtype, T, d, V, K, chunk):
     x = make_small(T, d, V, K, tau=1.5, dtype=dtype, seed=11, mask="random", mask_frac=0.1)
     dev = to_device(x)
@@ -69,6 +71,32 @@ def test_loss_writes_stay_in_bounds(dtype, T, d, V, K, chunk):
     assert rel(loss.item(), ref["loss"]) <= tol["loss"]
     assert rel_max(dH.float().cpu().numpy(), ref["dH"]) <= tol["grad"]
     assert rel_max(dW.cpu().numpy(), ref["dW"]) <= tol["grad"]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("T,d,V,K,chunk", [(300, 64, 1000, 7, 128), (1000, 256, 50001, 20, 384),
+                                           (1300, 64, 201088, 100, 4096)])
+def test_noalloc_forward_writes_stay_in_bounds(dtype, T, d, V, K, chunk):
+    """fckl_forward_noalloc's outputs (loss, lse, per-row losses, status) between guarded
+    margins; the last shape makes the call shrink its chunk to fit its fixed scratch."""
+    x = make_small(T, d, V, K, tau=1.5, dtype=dtype, seed=12, mask="random", mask_frac=0.1)
+    dev = to_device(x)
+    bufs = dict(loss=Guarded(4), lse=Guarded(4 * T), rl=Guarded(4 * T), status=Guarded(4))
+    loss = bufs["loss"].view(torch.float32, ())
+    lse = bufs["lse"].view(torch.float32, (T,))
+    rl = bufs["rl"].view(torch.float32, (T,))
+    status = bufs["status"].view(torch.int32, ())
+    api.fckl_forward_noalloc(dev["H"], dev["W"], dev["topk_idx"], dev["topk_logits"], dev["valid"], x["cfg"].tau,
+                             chunk, loss, lse, rl, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for name, b in bufs.items():
+        assert b.margins_intact(), f"write outside {name}"
+    ref = oracle_of(x, want_grads=False)
+    tol = TOL[dtype]
+    assert rel(loss.item(), ref["loss"]) <= tol["loss"]
+    assert rel_max(lse.cpu().numpy(), ref["lse"]) <= tol["loss"]
+    assert rel_max(rl.cpu().numpy(), ref["row_loss"]) <= tol["loss"]
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
