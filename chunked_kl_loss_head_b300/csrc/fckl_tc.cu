@@ -84,6 +84,7 @@ struct Prob {
   int tiles;       // num_m * num_n
   int a_mn, b_mn;  // operand layouts (see the engine)
   int n_fastest;   // raster: consecutive tiles walk N (1) or M (0)
+  int group_m;     // M-fastest raster: tile rows per group (0: all), see raster()
   int bn;          // tile width: a multiple of 32 (of 64 for an MN-major B), at most 256
   int N;           // extent of N; with a K-major B the last tile narrows to what is left
 };
@@ -129,14 +130,26 @@ __device__ __forceinline__ void tile_cols(const Prob& q, TileRef& r) {
   if (!q.b_mn && q.N - r.n0 < q.bn) r.bn = (q.N - r.n0 + 31) & ~31;
 }
 
+// Tile t's position.  N fastest: row-major over (m, n).  M fastest: the tile rows are
+// taken in groups of group_m (the last group may be smaller), and within a group the tiles
+// walk M fastest, then N; so the CTAs working at one time share a few B tiles and at most
+// group_m tile rows of A, whatever M is.  (The forward's A is the chunk's hidden states:
+// a group of 16 pair tile rows is 4096 rows, 23.6 MB at d = 2880, which stays in L2 while
+// the vocabulary streams past it; a 16384-row chunk walked whole would cycle 94 MB.)
 __device__ __forceinline__ void raster(const Prob& q, int t, int& m_t, int& n_t) {
   if (q.n_fastest) {
     n_t = t % q.num_n;
     m_t = t / q.num_n;
-  } else {
-    m_t = t % q.num_m;
-    n_t = t / q.num_m;
+    return;
   }
+  const int gfull = q.group_m > 0 && q.group_m < q.num_m ? q.group_m : q.num_m;
+  const int per = gfull * q.num_n;
+  const int grp = t / per;
+  const int r = t - grp * per;
+  const int m0 = grp * gfull;
+  const int gm = q.num_m - m0 < gfull ? q.num_m - m0 : gfull;
+  m_t = m0 + r % gm;
+  n_t = r / gm;
 }
 
 template <int CG>
@@ -910,6 +923,7 @@ Prob make_prob(int64_t M, int64_t N, int64_t K, int bn, bool a_mn, bool b_mn, bo
   q.a_mn = a_mn;
   q.b_mn = b_mn;
   q.n_fastest = n_fastest;
+  q.group_m = 0;
   q.bn = bn;
   q.N = static_cast<int>(N);
   return q;
@@ -1043,6 +1057,8 @@ int pick_bn(int64_t N, bool b_mn) {
 // The loss runs every contraction on CTA pairs; the single-CTA engine serves the test hook
 // for operand layouts the pair engine does not take (an MN-major B).
 constexpr int kLossCG = 2;
+// Rows of the forward's tile-row groups (see raster()).
+constexpr int kFwdGroupRows = 4096;
 
 }  // namespace
 
@@ -1077,7 +1093,8 @@ cudaError_t tc_fwd_tiles(const void* Hc, const void* W, int64_t rows, int64_t d,
   if (!map_kmajor(&maps.a[0], Hc, d, rows, d, BM) || !map_kmajor(&maps.b[0], W, d, V, d, kTileV / kLossCG))
     return cudaErrorInvalidValue;
   FwdEpi e{rows, V, kLog2e / tau, sidx, K, zk, part, nvt, ctrl};
-  const Prob p = make_prob(rows, V, d, kTileV, false, false, false, kLossCG);
+  Prob p = make_prob(rows, V, d, kTileV, false, false, false, kLossCG);
+  p.group_m = kFwdGroupRows / (BM * kLossCG);
   return launch_tc<kLossCG>(maps, plain_geom(&p, 1), e, sched, num_sms, st);
 }
 
