@@ -22,6 +22,8 @@ PROTOTYPES = {
     "fckl_backward": (c_i32, [c_vp, c_vp, c_vp, c_vp, c_vp, c_i64, c_i64, c_i64, c_i32, c_f32, c_i64, c_i32,
                               c_vp, c_f32, c_vp, c_vp, c_vp, c_vp, c_sz, c_vp]),
     "fckl_get_error": (c_i32, [c_vp, c_vp]),
+    "fckl_loss_partials": (c_i32, [c_vp, c_sz, c_vp, c_vp]),
+    "fckl_loss_finish": (c_i32, [c_vp, c_vp, c_vp, c_vp, c_vp]),
     "fckl_status_string": (ctypes.c_char_p, [c_i32]),
     "fckl_launch_count": (c_i64, []),
     "fckl_profile_enable": (None, [ctypes.c_int]),

@@ -109,6 +109,19 @@ def fckl_forward_noalloc(H, W, topk_idx, topk_logits, valid, tau, chunk, loss, l
     _check(st, "fckl_forward_noalloc")
 
 
+def fckl_loss_partials(ws, partials, stream=None):
+    """partials (float64 [2] on the device) = (sum of loss_t over valid rows, N) of the last
+    fckl_forward on ws."""
+    _check(lib().fckl_loss_partials(_ptr(ws), ws.numel() * ws.element_size(), _ptr(partials), _stream(stream)),
+           "fckl_loss_partials")
+
+
+def fckl_loss_finish(total, local, loss, grad_scale, stream=None):
+    """loss = total[0] / total[1]; grad_scale = local[1] / total[1] (both 0 when total[1] is 0)."""
+    _check(lib().fckl_loss_finish(_ptr(total), _ptr(local), _ptr(loss), _ptr(grad_scale), _stream(stream)),
+           "fckl_loss_finish")
+
+
 def fckl_topk_extract(logits, K, topk_idx, topk_logits, stream=None):
     """Per row of logits [T, V] (float32 or bfloat16): the K largest values and their ids,
     value descending then id ascending, into topk_idx [T, K] int32 / topk_logits float32."""

@@ -168,6 +168,20 @@ __global__ void __launch_bounds__(kReduceThreads) grad_scale_kernel(const uint8_
   }
 }
 
+// Data-parallel partials of the last forward: the fp64 loss sum and N.
+__global__ void loss_partials_kernel(const Ctrl* ctrl, double* out) {
+  out[0] = ctrl->loss_sum;
+  out[1] = static_cast<double>(ctrl->n_valid);
+}
+
+// From the partials summed over ranks: the mean loss, and this rank's gradient scale
+// N_local / N_total, which turns the backward's g / (tau N_local) into g / (tau N_total).
+__global__ void loss_finish_kernel(const double* total, const double* local, float* loss, float* grad_scale) {
+  const double n = total[1];
+  *loss = n > 0.0 ? static_cast<float>(total[0] / n) : 0.f;
+  *grad_scale = n > 0.0 ? static_cast<float>(local[1] / n) : 0.f;
+}
+
 __global__ void f32_to_bf16_kernel(const float4* __restrict__ src, __nv_bfloat162* __restrict__ dst, int64_t n4) {
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n4;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -258,6 +272,17 @@ cudaError_t launch_loss_reduce(const float* row_loss, const uint8_t* valid, int6
 cudaError_t launch_grad_scale(const uint8_t* valid, int64_t T, float tau, float grad_loss, const float* grad_scale,
                               Ctrl* ctrl, cudaStream_t st) {
   grad_scale_kernel<<<1, kReduceThreads, 0, st>>>(valid, T, tau, grad_loss, grad_scale, ctrl);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_loss_partials(const Ctrl* ctrl, double* out, cudaStream_t st) {
+  loss_partials_kernel<<<1, 1, 0, st>>>(ctrl, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_loss_finish(const double* total, const double* local, float* loss, float* grad_scale,
+                               cudaStream_t st) {
+  loss_finish_kernel<<<1, 1, 0, st>>>(total, local, loss, grad_scale);
   return cudaGetLastError();
 }
 
