@@ -6,8 +6,14 @@
 One step = fckl_forward + fckl_backward over one batch of the workload (all
 T tokens): loss, per-row logsumexp, dH and dW.  Inputs are synthetic (seeded
 generators, shapes of the pages' workloads) and larger than the 126 MB L2.
-Prints one JSON line (rank 0).  Under torchrun each rank runs its own batch
-(weak scaling, no collective on the data path); the time is the max over ranks.
+Prints one JSON line (rank 0).  Under torchrun the batch is token-sharded: each
+rank holds T tokens of its own (weak scaling) and the whole lm_head weight, and
+every step sums the loss partials (loss sum, N) over ranks before the backward and
+dW after it (chunked_kl_loss_head_b300.dist, NCCL all-reduces inside the timed
+step); the time is the max over ranks.
+
+    python bench.py --path module ...   # the FusedChunkedKLLoss autograd module
+    python bench.py --path topk ...     # teacher top-K extraction
 """
 
 from __future__ import annotations
@@ -189,12 +195,17 @@ def dense_torch_step(H, W, idx, tl, valid, tau):
 DENSE_BYTES_PER_ELEM = 16
 
 
-def run_memory_curve(args, cfg):
-    """Peak device memory of one fused fwd+bwd (inputs, outputs and workspace included) as
-    the token count grows, next to the size of the one dense [T x V] bf16 tensor the
-    method never builds, and the same step done the dense way in plain PyTorch (peak
-    memory, time, loss) where it fits: the pages' isolated loss benchmark compares the two
-    this way (axbrief.com, "Quantifying the Efficiency Gain: 15.6x VRAM Reduction").  A
+def linear_bytes(T, d, K, elem):
+    """Bytes of one fwd+bwd that grow with the token count: H and dH (elem bytes each), the
+    teacher cache (ids and logits, 4 bytes each), the valid mask, lse and the per-row losses
+    the workspace holds."""
+    return T * (2 * d * elem + 2 * K * 4 + 1 + 4 + 4)
+
+
+def memory_point(c, chunk, dense=True, timing=True):
+    """One point of the memory curve: the peak device memory of one fused fwd+bwd of
+    workload `c` (inputs, outputs and workspace included), optionally its time, and, where
+    it fits, the same step done the dense way in plain PyTorch (peak memory, time, loss).  A
     dense point whose predicted peak exceeds 80% of the free device memory is not run (no
     out-of-memory attempts); its prediction is reported instead."""
     import torch
@@ -203,64 +214,80 @@ def run_memory_curve(args, cfg):
     from chunked_kl_loss_head_b300.memory import dense_logit_bytes
     from gen import make_inputs
 
+    dev = torch.device("cuda", torch.cuda.current_device())
+    T = c.T
+    x = make_inputs(c)
+    tdt = torch.bfloat16 if c.dtype == "bf16" else torch.float32
+
+    def to_dev(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
+    torch.cuda.reset_peak_memory_stats(dev)
+    free0, _ = torch.cuda.mem_get_info(dev)
+    g = {k: to_dev(x[k]) for k in ("H", "W", "topk_idx", "topk_logits", "valid")}
+    del x
+    ws = api.workspace(T, c.d, c.V, c.K, chunk, tdt, dev)
+    loss, lse = api.forward(g["H"], g["W"], g["topk_idx"], g["topk_logits"], g["valid"], c.tau, chunk, ws=ws)
+    dH, dW = api.backward(g["H"], g["W"], g["topk_idx"], g["topk_logits"], g["valid"], lse, c.tau, chunk, ws=ws)
+    torch.cuda.synchronize(dev)
+    status = api.fckl_get_error(ws)
+    if status != 0:
+        raise RuntimeError(f"device status: {api.fckl_status_string(status)}")
+    peak = torch.cuda.max_memory_allocated(dev)
+    free1, _ = torch.cuda.mem_get_info(dev)
+    elem = 2 if c.dtype == "bf16" else 4
+    pt = dict(T=T, peak_device_gib=peak / 2 ** 30,
+              nontorch_device_gib=max(0.0, (free0 - free1 - peak) / 2 ** 30),
+              workspace_gib=ws.numel() / 2 ** 30, loss=float(loss.item()),
+              linear_gib=linear_bytes(T, c.d, c.K, elem) / 2 ** 30,
+              W_and_dW_gib=c.V * c.d * (elem + 4) / 2 ** 30,
+              dense_TxV_bf16_gib=dense_logit_bytes(T, c.V) / 2 ** 30)
+    if timing:
+        pt["fused_ms"] = time_ms(lambda: (api.forward(g["H"], g["W"], g["topk_idx"], g["topk_logits"], g["valid"],
+                                                      c.tau, chunk, ws=ws)[1],
+                                          api.backward(g["H"], g["W"], g["topk_idx"], g["topk_logits"], g["valid"],
+                                                       lse, c.tau, chunk, ws=ws)), dev)
+    del ws, loss, lse, dH, dW
+    if dense:
+        base = torch.cuda.memory_allocated(dev)
+        predicted = base + DENSE_BYTES_PER_ELEM * T * c.V
+        torch.cuda.empty_cache()
+        free2, _ = torch.cuda.mem_get_info(dev)
+        pt["dense_predicted_gib"] = predicted / 2 ** 30
+        if predicted - base > 0.8 * free2:
+            pt["dense"] = "not run: predicted peak above 80% of free device memory"
+        else:
+            torch.cuda.reset_peak_memory_stats(dev)
+            dl, _, _ = dense_torch_step(g["H"], g["W"], g["topk_idx"], g["topk_logits"], g["valid"], c.tau)
+            torch.cuda.synchronize(dev)
+            pt["dense_peak_device_gib"] = torch.cuda.max_memory_allocated(dev) / 2 ** 30
+            pt["dense_loss"] = float(dl.item())
+            if timing:
+                pt["dense_ms"] = time_ms(lambda: dense_torch_step(g["H"], g["W"], g["topk_idx"], g["topk_logits"],
+                                                                  g["valid"], c.tau), dev)
+    del g
+    torch.cuda.empty_cache()
+    return pt
+
+
+def run_memory_curve(args, cfg):
+    """Peak device memory of one fused fwd+bwd (inputs, outputs and workspace included) as
+    the token count grows, next to the size of the one dense [T x V] bf16 tensor the
+    method never builds, and the same step done the dense way in plain PyTorch (peak
+    memory, time, loss) where it fits: the pages' isolated loss benchmark compares the two
+    this way (axbrief.com, "Quantifying the Efficiency Gain: 15.6x VRAM Reduction")."""
+    import torch
+
     torch.cuda.set_device(0)
-    dev = torch.device("cuda", 0)
     chunk = args.chunk or cfg.chunks[0]
     points = []
     for T in (int(v) for v in args.memory_curve.split(",")):
         c = cfg.with_(name=f"{cfg.name}[T={T}]", T=T, seq_len=min(cfg.seq_len or T, T))
-        x = make_inputs(c)
-        tdt = torch.bfloat16 if c.dtype == "bf16" else torch.float32
-
-        def to_dev(a):
-            if a.dtype == np.uint16:
-                return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
-            return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
-
-        torch.cuda.synchronize(dev)
-        torch.cuda.empty_cache()
-        torch.cuda.reset_peak_memory_stats(dev)
-        free0, _ = torch.cuda.mem_get_info(dev)
-        g = {k: to_dev(x[k]) for k in ("H", "W", "topk_idx", "topk_logits", "valid")}
-        del x
-        ws = api.workspace(T, c.d, c.V, c.K, chunk, tdt, dev)
-        loss, lse = api.forward(g["H"], g["W"], g["topk_idx"], g["topk_logits"], g["valid"], c.tau, chunk, ws=ws)
-        dH, dW = api.backward(g["H"], g["W"], g["topk_idx"], g["topk_logits"], g["valid"], lse, c.tau, chunk,
-                              ws=ws)
-        torch.cuda.synchronize(dev)
-        status = api.fckl_get_error(ws)
-        if status != 0:
-            raise SystemExit(f"device status: {api.fckl_status_string(status)}")
-        peak = torch.cuda.max_memory_allocated(dev)
-        free1, _ = torch.cuda.mem_get_info(dev)
-        fused_ms = time_ms(lambda: (api.forward(g["H"], g["W"], g["topk_idx"], g["topk_logits"], g["valid"],
-                                                c.tau, chunk, ws=ws)[1],
-                                    api.backward(g["H"], g["W"], g["topk_idx"], g["topk_logits"], g["valid"],
-                                                 lse, c.tau, chunk, ws=ws)), dev)
-        pt = dict(T=T, peak_device_gib=peak / 2 ** 30,
-                  nontorch_device_gib=max(0.0, (free0 - free1 - peak) / 2 ** 30),
-                  workspace_gib=ws.numel() / 2 ** 30, loss=float(loss.item()), fused_ms=fused_ms,
-                  dense_TxV_bf16_gib=dense_logit_bytes(T, c.V) / 2 ** 30)
-        del ws, loss, lse, dH, dW
-        if not args.no_dense:
-            base = torch.cuda.memory_allocated(dev)
-            predicted = base + DENSE_BYTES_PER_ELEM * T * c.V
-            torch.cuda.empty_cache()
-            free2, _ = torch.cuda.mem_get_info(dev)
-            pt["dense_predicted_gib"] = predicted / 2 ** 30
-            if predicted - base > 0.8 * free2:
-                pt["dense"] = "not run: predicted peak above 80% of free device memory"
-            else:
-                torch.cuda.reset_peak_memory_stats(dev)
-                dl, _, _ = dense_torch_step(g["H"], g["W"], g["topk_idx"], g["topk_logits"], g["valid"], c.tau)
-                torch.cuda.synchronize(dev)
-                pt["dense_peak_device_gib"] = torch.cuda.max_memory_allocated(dev) / 2 ** 30
-                pt["dense_loss"] = float(dl.item())
-                pt["dense_ms"] = time_ms(lambda: dense_torch_step(g["H"], g["W"], g["topk_idx"], g["topk_logits"],
-                                                                  g["valid"], c.tau), dev)
-        points.append(pt)
-        del g
-        torch.cuda.empty_cache()
+        points.append(memory_point(c, chunk, dense=not args.no_dense))
     print(json.dumps(dict(metric="peak device GiB of one fused fwd+bwd vs tokens", unit="GiB",
                           config=dict(workload=cfg.name, d=cfg.d, V=cfg.V, K=cfg.K, chunk=chunk),
                           points=points)), flush=True)
@@ -354,6 +381,82 @@ def run_topk(args, cfg):
     print(json.dumps(line), flush=True)
 
 
+def run_module(args, cfg):
+    """The user's entry point, the FusedChunkedKLLoss autograd module: forward and backward
+    through autograd (hidden states and lm_head weight as leaf tensors of the workload's
+    dtype), gradients landing in .grad in that dtype.  Reports tokens/s and the peak device
+    memory of the timed steps (inputs, gradients, the module's workspace and its float32
+    dW before the cast)."""
+    import torch
+
+    from chunked_kl_loss_head_b300 import FusedChunkedKLLoss, api
+    from gen import make_inputs
+
+    if args.warmup < 3:
+        args.warmup = 3
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    chunk = args.chunk or cfg.chunks[0]
+    peaks = load_peaks()
+    x = make_inputs(cfg)
+    n_valid = int(x["valid"].sum())
+
+    def to_dev(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    g = {k: to_dev(x[k]) for k in ("H", "W", "topk_idx", "topk_logits", "valid")}
+    del x
+    H = g["H"].requires_grad_(True)
+    W = g["W"].requires_grad_(True)
+    mod = FusedChunkedKLLoss(tau=cfg.tau, chunk=chunk)
+
+    def step():
+        H.grad = None
+        W.grad = None
+        loss = mod(H, W, g["topk_idx"], g["topk_logits"], g["valid"])
+        loss.backward()
+        return loss
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    H.grad = None
+    W.grad = None
+    torch.cuda.reset_peak_memory_stats(dev)
+    launches0 = api.fckl_launch_count()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler("0") as clk:
+        torch.cuda.synchronize(dev)
+        e0.record()
+        for _ in range(args.steps):
+            loss = step()
+        e1.record()
+        torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / args.steps
+    launches = api.fckl_launch_count() - launches0
+    peak = torch.cuda.max_memory_allocated(dev)
+    T, d, V = cfg.T, cfg.d, cfg.V
+    flops = algorithmic_flops(T, d, V, n_valid)
+    tflops = flops / (ms / 1e3) / 1e12
+    peak_burst = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    elem = 2 if cfg.dtype == "bf16" else 4
+    line = dict(metric="FusedChunkedKLLoss module fwd+bwd tokens/s", value=T / (ms / 1e3), unit="tokens/s", n_gpus=1,
+                steps=args.steps, warmup=args.warmup, ms_per_step=ms, higher_is_better=True, scaling="weak",
+                vs_baseline=None, dtype=cfg.dtype, data="synthetic",
+                config=dict(workload=cfg.name, T=T, d=d, V=V, K=cfg.K, tau=cfg.tau, chunk=chunk,
+                            l2="inputs larger than L2"),
+                tflops=tflops, frac_bf16_peak=tflops / peak_burst, peak_device_gib=peak / 2 ** 30,
+                memory_parts_gib=dict(inputs=sum(t.numel() * t.element_size() for t in g.values()) / 2 ** 30,
+                                      grads=(T * d + V * d) * elem / 2 ** 30,
+                                      dW_float32=V * d * 4 / 2 ** 30,
+                                      workspace=api.fckl_workspace_size(T, d, V, cfg.K, chunk, H.dtype) / 2 ** 30,
+                                      dense_TxV_bf16=T * V * 2 / 2 ** 30),
+                loss=float(loss.item()), gpu_launches=int(launches), clocks=clk.summary())
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -368,8 +471,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--topk-rows", type=int, default=4096, help="rows of the --path topk workload")
-    ap.add_argument("--path", default="loss", choices=["loss", "topk"],
-                    help="topk: time the teacher top-K extraction instead (one JSON line)")
+    ap.add_argument("--path", default="loss", choices=["loss", "topk", "module"],
+                    help="topk: time the teacher top-K extraction instead; module: the FusedChunkedKLLoss "
+                         "autograd module (one JSON line)")
     ap.add_argument("--no-dense", action="store_true", help="--memory-curve without the dense PyTorch arm")
     ap.add_argument("--memory-curve", default="",
                     help="comma-separated token counts: peak device memory of one fwd+bwd of the workload's "
@@ -391,6 +495,9 @@ def main():
         return
     if args.path == "topk":
         run_topk(args, cfg)
+        return
+    if args.path == "module":
+        run_module(args, cfg)
         return
     if args.warmup < 3:
         args.warmup = 3  # timing rule: at least three warm-up steps
@@ -435,11 +542,24 @@ def main():
     dW = torch.empty((V, d), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step(src):
-        api.fckl_forward(src["H"], src["W"], src["topk_idx"], src["topk_logits"], src["valid"], cfg.tau, chunk,
-                         loss, lse, None, ws, stream)
-        api.fckl_backward(src["H"], src["W"], src["topk_idx"], src["topk_logits"], src["valid"], cfg.tau, chunk,
-                          lse, 1.0, dH, dW, ws, None, stream)
+    if world > 1:
+        # token-sharded: the loss partials and dW are summed over ranks inside the step
+        from chunked_kl_loss_head_b300.dist import ShardedKL
+
+        del ws, lse, dH, dW
+        sharded = ShardedKL(cfg.tau, chunk)
+
+        def step(src):
+            out = sharded.forward(src["H"], src["W"], src["topk_idx"], src["topk_logits"], src["valid"])
+            sharded.backward(1.0)
+            return out
+    else:
+        def step(src):
+            api.fckl_forward(src["H"], src["W"], src["topk_idx"], src["topk_logits"], src["valid"], cfg.tau, chunk,
+                             loss, lse, None, ws, stream)
+            api.fckl_backward(src["H"], src["W"], src["topk_idx"], src["topk_logits"], src["valid"], cfg.tau, chunk,
+                              lse, 1.0, dH, dW, ws, None, stream)
+            return loss
 
     def barrier():
         torch.cuda.synchronize(dev)
@@ -449,6 +569,8 @@ def main():
 
     for _ in range(args.warmup):
         step(g)
+    if world > 1:
+        ws = sharded.ops.ws
     status = api.fckl_get_error(ws)
     if status != 0:
         raise SystemExit(f"device status after warm-up: {api.fckl_status_string(status)}")
@@ -465,7 +587,7 @@ def main():
         barrier()
         e0.record(stream)
         for _ in range(args.steps):
-            step(g)
+            last = step(g)
         e1.record(stream)
         barrier()
     api.fckl_profile_enable(False)
@@ -478,7 +600,7 @@ def main():
     t_max = max_over_ranks(ms, dist, dev)
     peak_alloc = torch.cuda.max_memory_allocated(dev)
     free1, _ = torch.cuda.mem_get_info(dev)
-    loss_val = float(loss.item())
+    loss_val = float(last.item())
 
     sec_per_step = t_max / 1e3 / args.steps
     tokens_per_s = job_rate(T, world, sec_per_step)
@@ -558,14 +680,16 @@ def main():
             if i + 1 < n_e2e:
                 upload(1 - j)
             stream.wait_event(copied[j])
-            step(bufs[j])
+            out = step(bufs[j])
             used[j].record(stream)
-            loss_host[i].copy_(loss, non_blocking=True)
+            loss_host[i].copy_(out, non_blocking=True)
         stream.synchronize()
         barrier()
         e2e_s = max_over_ranks((time.perf_counter() - t0) / n_e2e, dist, dev)
         e2e = dict(value=job_rate(T, world, e2e_s), unit="tokens/s", h2d_bytes_per_step=int(h2d), d2h_bytes_per_step=4,
-                   ms_per_step=1e3 * e2e_s, steps=n_e2e, overlap="next step's input copy under this step's compute")
+                   ms_per_step=1e3 * e2e_s, steps=n_e2e, overlap="next step's input copy under this step's compute",
+                   outputs="the loss is read back each step; dH and dW stay on the device for the training "
+                           "step that consumes them")
         del bufs, pinned
 
     # ---- CPU baseline: the oracle on a bounded sample, rank 0 at N = 1 only
@@ -585,7 +709,8 @@ def main():
                     config=dict(workload=cfg.name, T=T, d=d, V=V, K=K, tau=cfg.tau, chunk=chunk, valid_rows=n_valid,
                                 batch=cfg.batch, seq_len=cfg.seq_len or T,
                                 l2="inputs larger than L2 (H %.2f GB, W %.2f GB)" % (T * d * 2 / 1e9, V * d * 2 / 1e9),
-                                parallelism=f"replicas x{world}"),
+                                parallelism=(f"dp{world}: token-sharded, loss partials and dW all-reduced "
+                                             "(NCCL) inside the step" if world > 1 else "one GPU")),
                     tflops=tflops, frac_bf16_peak=tflops / peak_burst,
                     frac_bf16_peak_sustained=tflops / peak_sust, peak_source=peaks["source"],
                     peak_device_gib=peak_alloc / 2 ** 30, nontorch_device_gib=max(0.0, (free0 - free1 - peak_alloc) / 2 ** 30),

@@ -2,11 +2,10 @@
 order (value descending, id ascending) makes the answer unique, so ids and values must
 match exactly.  The cases reach every path of the kernel: rows short enough to keep
 whole, the sampled threshold on long rows, the exact radix-select path (forced by heavy
-ties and by rows whose entries are all equal), rows that start off a 16-byte boundary
-(entries before the first and after the last aligned 16-byte block are read apart from
-the bulk-copied body), rows with no aligned block at all, bodies that end inside a copy
-chunk and rows long enough to reuse every ring slot many times, K = 1 and K = V, signed
-zeros and infinities."""
+ties and by rows whose entries are all equal), rows whose start is 16-byte aligned (read
+with 16-byte vector loads, four in flight per thread, plus a short tail of fewer than one
+vector) and rows whose start is not (read entry by entry), rows of every length around
+the vector width, K = 1 and K = V, signed zeros and infinities."""
 
 import numpy as np
 import pytest
