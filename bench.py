@@ -468,6 +468,9 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=256, help="rows of the oracle CPU-baseline sample")
     ap.add_argument("--ref-rows", type=int, default=128, help="rows per reference-arm step")
     ap.add_argument("--shape", default="", help="override T,d,V,K of the workload (e.g. a small ncu case)")
+    ap.add_argument("--dp", action="store_true",
+                    help="take the token-sharded path (NCCL process group, loss partials and dW all-reduced in "
+                         "the step) even with one process; under torchrun with N > 1 it is always taken")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--topk-rows", type=int, default=4096, help="rows of the --path topk workload")
@@ -510,9 +513,13 @@ def main():
     rank, local_rank, world = dist_env()
     torch.cuda.set_device(local_rank)
     dist = None
-    if world > 1:
+    sharded_path = world > 1 or args.dp
+    if sharded_path:
         import torch.distributed as dist
 
+        if "MASTER_ADDR" not in os.environ:  # one process, not under a launcher
+            os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=os.environ.get("MASTER_PORT", "29533"),
+                              RANK="0", WORLD_SIZE="1")
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     dev = torch.device("cuda", local_rank)
     chunk = args.chunk or cfg.chunks[0]
@@ -542,7 +549,7 @@ def main():
     dW = torch.empty((V, d), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    if world > 1:
+    if sharded_path:
         # token-sharded: the loss partials and dW are summed over ranks inside the step
         from chunked_kl_loss_head_b300.dist import ShardedKL
 
@@ -569,7 +576,7 @@ def main():
 
     for _ in range(args.warmup):
         step(g)
-    if world > 1:
+    if sharded_path:
         ws = sharded.ops.ws
     status = api.fckl_get_error(ws)
     if status != 0:
@@ -659,7 +666,7 @@ def main():
         pinned = {k: v.pin_memory() for k, v in h.items()}
         bufs = [{k: torch.empty_like(v, device=dev) for k, v in h.items()} for _ in range(2)]
         h2d = sum(v.numel() * v.element_size() for v in pinned.values())
-        n_e2e = max(1, min(args.steps, 5))
+        n_e2e = max(1, min(args.steps, 10))
         loss_host = torch.empty(n_e2e, dtype=torch.float32).pin_memory()
         copy_stream = torch.cuda.Stream(dev)
         copied = [torch.cuda.Event() for _ in range(2)]
@@ -710,7 +717,7 @@ def main():
                                 batch=cfg.batch, seq_len=cfg.seq_len or T,
                                 l2="inputs larger than L2 (H %.2f GB, W %.2f GB)" % (T * d * 2 / 1e9, V * d * 2 / 1e9),
                                 parallelism=(f"dp{world}: token-sharded, loss partials and dW all-reduced "
-                                             "(NCCL) inside the step" if world > 1 else "one GPU")),
+                                             "(NCCL) inside the step" if sharded_path else "one GPU")),
                     tflops=tflops, frac_bf16_peak=tflops / peak_burst,
                     frac_bf16_peak_sustained=tflops / peak_sust, peak_source=peaks["source"],
                     peak_device_gib=peak_alloc / 2 ** 30, nontorch_device_gib=max(0.0, (free0 - free1 - peak_alloc) / 2 ** 30),

@@ -104,3 +104,21 @@ def test_topk_rejects_bad_arguments():
         assert L.fckl_topk_extract(p, T, V, K, dt, p, p, None) == 1
     # misaligned logits for fp32
     assert L.fckl_topk_extract(ctypes.c_void_p((1 << 20) + 2), 4, 100, 10, F32, p, p, None) == 2
+
+
+def test_data_parallel_calls_reject_bad_arguments():
+    L = _lib.lib()
+    p = ctypes.c_void_p(1 << 20)
+    # partials: no workspace, a workspace off 256 bytes or too small, no or misaligned output
+    assert L.fckl_loss_partials(None, 1 << 20, p, None) == 3
+    assert L.fckl_loss_partials(ctypes.c_void_p((1 << 20) + 8), 1 << 20, p, None) == 3
+    assert L.fckl_loss_partials(p, 64, p, None) == 3
+    assert L.fckl_loss_partials(p, 1 << 20, None, None) == 1
+    assert L.fckl_loss_partials(p, 1 << 20, ctypes.c_void_p((1 << 20) + 4), None) == 1
+    # finish: any null pointer, or a misaligned one
+    for k in range(4):
+        args = [p, p, p, p]
+        args[k] = None
+        assert L.fckl_loss_finish(*args, None) == 1
+    assert L.fckl_loss_finish(ctypes.c_void_p((1 << 20) + 4), p, p, p, None) == 1
+    assert L.fckl_loss_finish(p, p, ctypes.c_void_p((1 << 20) + 2), p, None) == 1

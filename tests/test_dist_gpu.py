@@ -5,6 +5,12 @@ compared with the oracle on the whole batch: the loss on every shard, dH row by 
 and dW summed over the shards.  The collectives themselves (gloo on CPU) are covered by
 test_dist_sharded_cpu.py."""
 
+import json
+import os
+import socket
+import subprocess
+import sys
+
 import numpy as np
 import pytest
 import torch
@@ -61,3 +67,36 @@ def test_sharded_module_of_one_rank_is_the_module():
     ref = oracle_of(x, grad=0.5)
     assert rel(l1, ref["loss"]) <= TOL["bf16"]["loss"]
     assert rel_max(h1, ref["dH"]) <= TOL["bf16"]["grad"] and rel_max(w1, ref["dW"]) <= TOL["bf16"]["grad"]
+
+
+def _free_port():
+    with socket.socket() as sock:
+        sock.bind(("127.0.0.1", 0))
+        return sock.getsockname()[1]
+
+
+def _bench_line(args, torchrun=False):
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    cmd = [sys.executable]
+    if torchrun:
+        cmd += ["-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "1", "--master-addr", "127.0.0.1",
+                "--master-port", str(_free_port())]
+    cmd += [os.path.join(root, "bench.py")] + args
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=600, cwd=root)
+    assert r.returncode == 0, r.stderr[-3000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout[-2000:]
+    return json.loads(lines[0])
+
+
+def test_bench_sharded_path_under_torchrun():
+    """bench.py's token-sharded step on the GPU: an NCCL process group (one rank here) with
+    the loss partials and dW all-reduced inside the timed step, against the direct path
+    on the same workload: the same loss."""
+    args = ["--shape", "8192,2880,201088,100", "--steps", "2", "--warmup", "3", "--no-e2e", "--no-cpu"]
+    dp = _bench_line(args + ["--dp"], torchrun=True)
+    one = _bench_line(args)
+    print(dp["config"]["parallelism"], dp["value"], one["value"], dp["loss"], one["loss"])
+    assert dp["config"]["parallelism"].startswith("dp1")
+    assert dp["value"] > 0 and dp["gpu_launches"] > one["gpu_launches"]  # + partials and finish
+    assert dp["loss"] == one["loss"]
