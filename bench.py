@@ -70,7 +70,7 @@ def max_over_ranks(x, dist=None, device="cpu"):
 
 def job_rate(units_per_rank, world, seconds):
     """Whole-job throughput when every rank processes its own batch of `units_per_rank`
-    (token-sharded replicas, weak scaling)."""
+    (token-sharded, weak scaling)."""
     return world * units_per_rank / seconds
 
 

@@ -26,10 +26,10 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// Teacher preparation, one warp per row (the teacher's top-K cache, getaibook.com,
-// "Preparing Offline Top-K Logits"): p = softmax(topk_logits / tau) over the K cached
-// ids, log p alongside, and the (id, p, log p) triples sorted by id so the logit-tile
-// epilogues can walk a row's ids in vocabulary order.  Ids outside [0, V) are recorded
+// Teacher preparation for any K up to FCKL_MAX_K, one warp per row (the teacher's top-K
+// cache, getaibook.com, "Preparing Offline Top-K Logits"): p = softmax(topk_logits / tau)
+// over the K cached ids, log p alongside, and the (id, p, log p) triples sorted by id so
+// the logit-tile epilogues can walk a row's ids in vocabulary order.  Ids outside [0, V) are recorded
 // as FCKL_ERR_BAD_INDEX and replaced by INT32_MAX with p = 0, so no later step can use
 // them as an address or match them to a column.  zk (the student logits at the ids) is
 // cleared for the forward tiles to fill.
@@ -78,6 +78,129 @@ __global__ void prep_kernel(const int32_t* __restrict__ idx, const float* __rest
     sp[o] = (id == INT32_MAX) ? 0.f : expf(lp);
     zk[o] = 0.f;
   }
+}
+
+// The same preparation for K <= 128, with the ids sorted by a bitonic network in registers
+// instead of ranked by K compares each.  A row's K (id, k) pairs become keys id * 128 + k
+// (so equal ids keep their cached order), padded with all-ones keys that sort last, P keys
+// per lane (32 P >= K slots).  Key slot e = P * lane + i holds register i of its lane: the
+// network's exchanges across P slots or more are shuffles between lanes, shorter ones are
+// swaps between a lane's own registers.  Below V = 2^24 - 1 a key fits 32 bits (bad ids as
+// 2^24 - 1, after every valid id); otherwise it is 64 bits wide (bad ids as INT32_MAX).
+// The sorted keys then pass through shared memory so that the row's outputs are written
+// with consecutive lanes on consecutive ids.
+constexpr int kPrepWarps = 4;
+constexpr int kSmallK = 128;
+constexpr int64_t kKey32MaxV = (int64_t(1) << 24) - 1;  // V below this: 32-bit keys
+
+__device__ __forceinline__ uint32_t shfl_xor_key(uint32_t v, int m) { return __shfl_xor_sync(kFull, v, m); }
+__device__ __forceinline__ uint64_t shfl_xor_key(uint64_t v, int m) {
+  return __shfl_xor_sync(kFull, static_cast<unsigned long long>(v), m);
+}
+
+template <int P, class Key>
+__global__ void __launch_bounds__(kPrepWarps * 32) prep_small_kernel(
+    const int32_t* __restrict__ idx, const float* __restrict__ logits, int64_t rows, int K, int64_t V, float tau,
+    int32_t* __restrict__ sidx, float* __restrict__ sp, float* __restrict__ slogp, float* __restrict__ zk,
+    Ctrl* ctrl) {
+  constexpr int N = 32 * P;
+  constexpr bool kWide = sizeof(Key) == 8;
+  constexpr uint32_t kBadId = kWide ? uint32_t(INT32_MAX) : uint32_t(kKey32MaxV);
+  constexpr int kShift = kWide ? 32 : 7;
+  __shared__ float sh_lp[kPrepWarps][N];
+  __shared__ Key sh_key[kPrepWarps][N];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kPrepWarps + warp;
+  if (row >= rows) return;
+  const int32_t* irow = idx + row * K;
+  const float* lrow = logits + row * K;
+
+  float a[P];
+  Key key[P];
+  float amax = -INFINITY;
+  bool bad = false;
+#pragma unroll
+  for (int i = 0; i < P; ++i) {
+    const int k = i * 32 + lane;
+    a[i] = -INFINITY;
+    key[i] = ~Key(0);
+    if (k < K) {
+      const int32_t id = irow[k];
+      uint32_t kid = static_cast<uint32_t>(id);
+      if (id < 0 || static_cast<int64_t>(id) >= V) {
+        bad = true;
+        kid = kBadId;
+      }
+      a[i] = lrow[k] / tau;
+      amax = fmaxf(amax, a[i]);
+      key[i] = (static_cast<Key>(kid) << kShift) | static_cast<Key>(k);
+    }
+  }
+  if (__any_sync(kFull, bad) && lane == 0) set_status(ctrl, FCKL_ERR_BAD_INDEX);
+  amax = warp_max(amax);
+  float sum = 0.f;
+#pragma unroll
+  for (int i = 0; i < P; ++i)
+    if (i * 32 + lane < K) sum += expf(a[i] - amax);
+  sum = warp_sum(sum);
+  const float lse_a = amax + logf(sum);
+#pragma unroll
+  for (int i = 0; i < P; ++i)
+    if (i * 32 + lane < K) sh_lp[warp][i * 32 + lane] = a[i] - lse_a;
+
+#pragma unroll
+  for (int size = 2; size <= N; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      if (stride >= P) {
+#pragma unroll
+        for (int i = 0; i < P; ++i) {
+          const int e = lane * P + i;
+          const Key p = shfl_xor_key(key[i], stride / P);
+          const bool keep_min = ((e & stride) == 0) == ((e & size) == 0);
+          key[i] = keep_min ? (p < key[i] ? p : key[i]) : (p > key[i] ? p : key[i]);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < P; ++i) {
+          if (i & stride) continue;
+          const int j = i | stride;
+          const Key lo = key[i] < key[j] ? key[i] : key[j];
+          const Key hi = key[i] < key[j] ? key[j] : key[i];
+          const bool asc = ((lane * P + i) & size) == 0;
+          key[i] = asc ? lo : hi;
+          key[j] = asc ? hi : lo;
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < P; ++i) sh_key[warp][lane * P + i] = key[i];
+  __syncwarp();
+  for (int e = lane; e < K; e += 32) {
+    const Key kk = sh_key[warp][e];
+    const uint32_t kid = static_cast<uint32_t>(kk >> kShift);
+    const int32_t id = kid == kBadId ? INT32_MAX : static_cast<int32_t>(kid);
+    const float lp = sh_lp[warp][static_cast<uint32_t>(kk) & (kWide ? 0xffffffffu : 0x7fu)];
+    const int64_t o = row * K + e;
+    sidx[o] = id;
+    slogp[o] = lp;
+    sp[o] = (id == INT32_MAX) ? 0.f : expf(lp);
+    zk[o] = 0.f;
+  }
+}
+
+template <int P>
+cudaError_t launch_prep_small(const int32_t* idx, const float* logits, int64_t rows, int32_t K, int64_t V,
+                              float tau, ChunkScratch s, Ctrl* ctrl, cudaStream_t st) {
+  const unsigned grid = static_cast<unsigned>((rows + kPrepWarps - 1) / kPrepWarps);
+  if (V < kKey32MaxV)
+    prep_small_kernel<P, uint32_t><<<grid, kPrepWarps * 32, 0, st>>>(idx, logits, rows, K, V, tau, s.sidx, s.sp,
+                                                                     s.slogp, s.zk, ctrl);
+  else
+    prep_small_kernel<P, uint64_t><<<grid, kPrepWarps * 32, 0, st>>>(idx, logits, rows, K, V, tau, s.sidx, s.sp,
+                                                                     s.slogp, s.zk, ctrl);
+  return cudaGetLastError();
 }
 
 // One warp per row: merge the (max, sum) partials of every 256-wide vocab tile into the
@@ -247,6 +370,9 @@ cudaError_t launch_transpose_bf16(const void* in, int64_t rows, int64_t cols, in
 
 cudaError_t launch_prep(const int32_t* idx, const float* logits, int64_t rows, int32_t K, int64_t V,
                         float tau, ChunkScratch s, Ctrl* ctrl, cudaStream_t st) {
+  if (K <= 32) return launch_prep_small<1>(idx, logits, rows, K, V, tau, s, ctrl, st);
+  if (K <= 64) return launch_prep_small<2>(idx, logits, rows, K, V, tau, s, ctrl, st);
+  if (K <= kSmallK) return launch_prep_small<4>(idx, logits, rows, K, V, tau, s, ctrl, st);
   constexpr int warps = 4;
   const unsigned grid = static_cast<unsigned>((rows + warps - 1) / warps);
   prep_kernel<<<grid, warps * 32, warps * K * sizeof(int32_t), st>>>(idx, logits, rows, K, V, tau, s.sidx, s.sp,

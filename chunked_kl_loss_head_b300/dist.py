@@ -100,16 +100,21 @@ class ShardedKL:
         self._saved = dict(H=H, W=W, topk_idx=topk_idx, topk_logits=topk_logits, valid=valid, lse=lse, local=local)
         return local
 
+    def _state(self, need_scale=False):
+        if self._saved is None or (need_scale and "grad_scale" not in self._saved):
+            raise RuntimeError("ShardedKL: run forward_local and finish (or forward) before this step")
+        return self._saved
+
     def finish(self, total):
         """From the partials summed over ranks: the mean loss over every rank's valid rows."""
-        loss, scale = self.ops.finish(total, self._saved["local"])
+        loss, scale = self.ops.finish(total, self._state()["local"])
         self._saved["grad_scale"] = scale
         return loss
 
     def backward_local(self, grad_loss=1.0, grad_scale=None):
         """(dH, dW) of this rank's rows for the loss over all ranks; dW before the sum over
         ranks.  grad_scale (device float32 scalar, optional) multiplies grad_loss."""
-        s = self._saved
+        s = self._state(need_scale=True)
         scale = s["grad_scale"] if grad_scale is None else grad_scale * s["grad_scale"]
         return self.ops.backward_local(s["H"], s["W"], s["topk_idx"], s["topk_logits"], s["valid"], s["lse"],
                                        grad_loss, scale)
@@ -135,11 +140,16 @@ class _ShardedFn(torch.autograd.Function):
     def forward(ctx, H, W, topk_idx, topk_logits, valid, sharded):
         ctx.sharded = sharded
         ctx.w_dtype = W.dtype
-        return sharded.forward(H, W, topk_idx, topk_logits, valid)
+        loss = sharded.forward(H, W, topk_idx, topk_logits, valid)
+        # this call's own state: another forward through the same object (a second
+        # micro-batch) may come before this call's backward
+        ctx.state = dict(sharded._saved)
+        return loss
 
     @staticmethod
     def backward(ctx, grad):
         g = grad.detach().to(torch.float32).reshape(())
+        ctx.sharded._saved = ctx.state
         dH, dW = ctx.sharded.backward(1.0, g)
         if ctx.w_dtype != torch.float32:
             dW = dW.to(ctx.w_dtype)

@@ -1,9 +1,10 @@
-"""The multi-process path of bench.py on CPU (gloo, two ranks).
+"""The multi-process timing logic of bench.py on CPU (gloo, two ranks).
 
-On one GPU per box the benchmark runs token-sharded replicas: every rank times its own
-batch and the job's time is the slowest rank's, with no collective on the data path.
-These tests run that host logic with two gloo ranks, and launch the reference arm under
-torchrun with two processes (rank 0 alone works and prints one line)."""
+Under torchrun every rank of the benchmark runs T tokens of its own (weak scaling), and
+the job's time is the slowest rank's.  These tests run that host logic (the max over
+ranks and the whole-job rate) with two gloo ranks, and launch the reference arm under
+torchrun with two processes (rank 0 alone works and prints one line).  The token-sharded
+loss itself, with its all-reduces, is covered by test_dist_sharded_cpu.py."""
 
 import json
 import os

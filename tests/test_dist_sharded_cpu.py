@@ -127,3 +127,42 @@ def test_sharded_loss_matches_whole_batch(world, all_ignored_rank, use_module):
         assert loss == pytest.approx(ref["loss"], rel=1e-12, abs=0)
         np.testing.assert_allclose(dH, ref["dH"][a:b], rtol=1e-10, atol=1e-15)
         np.testing.assert_allclose(dW, ref["dW"], rtol=1e-10, atol=1e-15)
+
+
+def test_phases_out_of_order_are_refused():
+    sys.path.insert(0, ROOT)
+    from chunked_kl_loss_head_b300.dist import ShardedKL
+
+    sh = ShardedKL(ops=OracleOps(1.0), reduce=lambda t: None)
+    with pytest.raises(RuntimeError):
+        sh.backward_local()
+    with pytest.raises(RuntimeError):
+        sh.finish(torch.zeros(2, dtype=torch.float64))
+
+
+def test_two_micro_batches_before_one_backward():
+    """Two forwards through one sharded object, then one backward of their sum: each call's
+    gradient uses its own rows (one rank; the sum over ranks is the identity)."""
+    sys.path.insert(0, ROOT)
+    from chunked_kl_loss_head_b300.dist import ShardedKL, _ShardedFn
+    from gen import make_small
+    from oracle import fwd_bwd
+
+    sh = ShardedKL(ops=OracleOps(1.2), reduce=lambda t: None)
+    W = torch.from_numpy(make_small(T=3, d=6, V=29, K=4, tau=1.2, dtype="f32", seed=9)["W"].astype(np.float64))
+    Wg = W.clone().requires_grad_(True)
+    xs, Hs, total = [], [], 0.0
+    for seed in (10, 11):
+        x = make_small(T=13, d=6, V=29, K=4, tau=1.2, dtype="f32", seed=seed, mask="random", mask_frac=0.2)
+        H = torch.from_numpy(x["H"].astype(np.float64)).requires_grad_(True)
+        total = total + _ShardedFn.apply(H, Wg, torch.from_numpy(x["topk_idx"]), torch.from_numpy(x["topk_logits"]),
+                                         torch.from_numpy(np.ascontiguousarray(x["valid"])), sh)
+        xs.append(x)
+        Hs.append(H)
+    total.backward()
+    dW = 0.0
+    for x, H in zip(xs, Hs):
+        ref = fwd_bwd(x["H"], W.numpy(), x["topk_idx"], x["topk_logits"], x["valid"], 1.2)
+        np.testing.assert_allclose(H.grad.numpy(), ref["dH"], rtol=1e-10, atol=1e-15)
+        dW = dW + ref["dW"]
+    np.testing.assert_allclose(Wg.grad.numpy(), dW, rtol=1e-10, atol=1e-15)

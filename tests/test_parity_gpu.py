@@ -163,6 +163,29 @@ def test_duplicate_ids_add_up(dtype):
     check(x, run_gpu(x, 16), label=f"{dtype} duplicate ids")
 
 
+@pytest.mark.parametrize("V", [(1 << 24) - 2, (1 << 24) + 5])
+@pytest.mark.parametrize("K", [10, 100])
+def test_vocabulary_at_the_24_bit_edge(V, K):
+    """Teacher preparation packs (id, position) into 32-bit sort keys below V = 2^24 - 1 and
+    into 64-bit keys from there on: both sides of the edge, with ids planted at the top of
+    the vocabulary and duplicated, through the whole loss."""
+    x = make_small(T=24, d=8, V=V, K=K, tau=1.3, dtype="bf16", seed=33, ids="uniform", mask="random", mask_frac=0.2)
+    x["topk_idx"][:, 0] = V - 1
+    x["topk_idx"][:, 1] = V - 2
+    x["topk_idx"][3, 2] = V - 1  # a duplicate
+    x["topk_idx"][5, 4] = x["topk_idx"][5, 3]
+    ref = oracle_of(x, row_block=4)
+    got = run_gpu(x, 16)
+    tol = TOL["bf16"]
+    assert got["status"] == 0
+    errs = dict(loss=rel(got["loss"], ref["loss"]), lse=rel_max(got["lse"], ref["lse"]),
+                row_loss=rel_max(got["row_loss"], ref["row_loss"]), dH=rel_max(got["dH"], ref["dH"]),
+                dW=rel_max(got["dW"], ref["dW"]))
+    print(V, K, {k: f"{v:.2e}" for k, v in errs.items()})
+    assert errs["loss"] <= tol["loss"] and errs["lse"] <= tol["loss"] and errs["row_loss"] <= tol["loss"], errs
+    assert errs["dH"] <= tol["grad"] and errs["dW"] <= tol["grad"], errs
+
+
 def test_grad_scale_and_grad_loss():
     x = make_small(T=256, d=64, V=800, K=5, tau=1.0, dtype="bf16", seed=11, mask="random", mask_frac=0.1)
     a = run_gpu(x, 128, grad_loss=2.5)
@@ -220,6 +243,30 @@ def test_autograd_module_bf16():
     assert rel(loss.item(), ref["loss"]) <= TOL["bf16"]["loss"]
     assert rel_max(H.grad.float().cpu().numpy(), ref["dH"]) <= TOL["bf16"]["grad"]
     assert rel_max(W.grad.float().cpu().numpy(), ref["dW"]) <= TOL["bf16"]["grad"]
+
+
+def test_autograd_module_two_micro_batches():
+    """Two calls of one module instance (different sizes, so its workspace is made anew for
+    the second), then one backward of their sum: each call's gradients against the oracle."""
+    from chunked_kl_loss_head_b300 import FusedChunkedKLLoss
+
+    mod = FusedChunkedKLLoss(tau=1.1, chunk=192)
+    xa = make_small(T=500, d=64, V=2000, K=7, tau=1.1, dtype="bf16", seed=16, mask="random", mask_frac=0.1)
+    xb = make_small(T=333, d=64, V=2000, K=7, tau=1.1, dtype="bf16", seed=17, mask="random", mask_frac=0.1)
+    xb["W"] = xa["W"]
+    da, db = to_device(xa), to_device(xb)
+    W = da["W"].clone().requires_grad_(True)
+    Ha = da["H"].clone().requires_grad_(True)
+    Hb = db["H"].clone().requires_grad_(True)
+    la = mod(Ha, W, da["topk_idx"], da["topk_logits"], da["valid"])
+    lb = mod(Hb, W, db["topk_idx"], db["topk_logits"], db["valid"])
+    (la + 2.0 * lb).backward()
+    ra, rb = oracle_of(xa), oracle_of(xb, grad=2.0)
+    tol = TOL["bf16"]
+    assert rel(la.item(), ra["loss"]) <= tol["loss"] and rel(lb.item(), rb["loss"]) <= tol["loss"]
+    assert rel_max(Ha.grad.float().cpu().numpy(), ra["dH"]) <= tol["grad"]
+    assert rel_max(Hb.grad.float().cpu().numpy(), rb["dH"]) <= tol["grad"]
+    assert rel_max(W.grad.float().cpu().numpy(), ra["dW"] + rb["dW"]) <= tol["grad"]
 
 
 def test_bounded_wait_reports_timeout():
