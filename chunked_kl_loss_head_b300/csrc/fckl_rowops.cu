@@ -203,9 +203,21 @@ cudaError_t launch_prep_small(const int32_t* idx, const float* logits, int64_t r
   return cudaGetLastError();
 }
 
+// Adds a (max, sum) partial q to a running (m, s) pair of the same base-2 units.
+__device__ __forceinline__ void merge_partial(float& m, float& s, float qm, float qs) {
+  if (qm > m) {
+    s = s * exp2f(m - qm) + qs;  // m = -inf at the start: 0 * 0 + qs
+    m = qm;
+  } else {
+    s += qs * exp2f(qm - m);
+  }
+}
+
 // One warp per row: merge the (max, sum) partials of every 256-wide vocab tile into the
 // row's logsumexp, then loss_t = sum_k p_k (log p_k - s_k + lse_t) with s_k = z_k / tau.
-// Partials are in base-2 units (u = z * log2(e) / tau).
+// Partials are in base-2 units (u = z * log2(e) / tau).  Each lane merges its share of the
+// partials as it reads them (two per 16-byte load when the rows start on 16-byte
+// boundaries), then the lanes merge theirs; one pass over the partials.
 __global__ void combine_kernel(const float2* __restrict__ part, int nvt, const float* __restrict__ zk,
                                const float* __restrict__ sp, const float* __restrict__ slogp,
                                const uint8_t* __restrict__ valid, int64_t rows, int K, float tau,
@@ -214,15 +226,29 @@ __global__ void combine_kernel(const float2* __restrict__ part, int nvt, const f
   const int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + warp;
   if (row >= rows) return;
   const float2* pr = part + row * nvt;
-  float m = -INFINITY;
-  for (int j = lane; j < nvt; j += 32) m = fmaxf(m, pr[j].x);
-  m = warp_max(m);
-  float s = 0.f;
-  for (int j = lane; j < nvt; j += 32) {
-    const float2 q = pr[j];
-    s += q.y * exp2f(q.x - m);
+  float m = -INFINITY, s = 0.f;
+  if ((nvt & 1) == 0 && (reinterpret_cast<uintptr_t>(part) & 15) == 0) {
+    const float4* p4 = reinterpret_cast<const float4*>(pr);
+    const int n4 = nvt >> 1;
+#pragma unroll 4
+    for (int j = lane; j < n4; j += 32) {
+      const float4 v = p4[j];
+      merge_partial(m, s, v.x, v.y);
+      merge_partial(m, s, v.z, v.w);
+    }
+  } else {
+    for (int j = lane; j < nvt; j += 32) {
+      const float2 q = pr[j];
+      merge_partial(m, s, q.x, q.y);
+    }
   }
-  s = warp_sum(s);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(kFull, m, o), s2 = __shfl_xor_sync(kFull, s, o);
+    const float mm = fmaxf(m, m2);
+    s = (mm == -INFINITY) ? 0.f : s * exp2f(m - mm) + s2 * exp2f(m2 - mm);
+    m = mm;
+  }
   const float l = (m + log2f(s)) * kLn2;
   float acc = 0.f;
   const bool ok = valid[row] != 0;
