@@ -271,6 +271,18 @@ __device__ __forceinline__ int lower_bound_ids(const int32_t* ids, int K, int64_
   return a;
 }
 
+// 2^x by the PTX ISA's approximate base-2 exponential, ex2.approx.ftz.f32 (subnormal
+// results flush to zero).  Its error, a few units in the last place of fp32, is far below
+// what the epilogues keep: the bf16 rounding of G, and sums of exponentials whose loss is
+// checked to 2e-3 against the fp64 oracle.  The exponentials are the epilogues' bulk of
+// instructions, and the epilogue warps share their sub-partitions with the TMA and MMA
+// issuing threads.
+__device__ __forceinline__ float ex2_fast(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ float pick32(const uint32_t (&v)[32], int j) {
   uint32_t x = v[0];
 #pragma unroll
@@ -323,18 +335,26 @@ struct FwdEpi {
       tmem_ld_wait();
       float u[32];
       float mx = -INFINITY;
+      if (n0 + c + 32 <= V) {  // a whole chunk of vocabulary columns (all but the last tile's end)
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        u[i] = (n0 + c + i < V) ? __uint_as_float(v[i]) * c2 : -INFINITY;
-        mx = fmaxf(mx, u[i]);
+        for (int i = 0; i < 32; ++i) {
+          u[i] = __uint_as_float(v[i]) * c2;
+          mx = fmaxf(mx, u[i]);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          u[i] = (n0 + c + i < V) ? __uint_as_float(v[i]) * c2 : -INFINITY;
+          mx = fmaxf(mx, u[i]);
+        }
       }
       if (mx > m_run) {
-        s_run *= exp2f(m_run - mx);
+        s_run *= ex2_fast(m_run - mx);
         m_run = mx;
       }
       float s = 0.f;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) s += exp2f(u[i] - m_run);
+      for (int i = 0; i < 32; ++i) s += ex2_fast(u[i] - m_run);
       s_run += s;
       while (nid < n0 + c + 32) {
         zk[row * K + k] = pick32(v, static_cast<int>(nid - (n0 + c)));
@@ -410,8 +430,13 @@ struct BwdEpi {
           uint32_t v[32];
           tmem_ld_32x32(taddr + c + 32 * h, v);
           tmem_ld_wait();
+          if (nc + 32 <= vend) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) g[i] = (nc + i < vend) ? exp2f(__uint_as_float(v[i]) * c2 - lse2) : 0.f;
+            for (int i = 0; i < 32; ++i) g[i] = ex2_fast(__uint_as_float(v[i]) * c2 - lse2);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) g[i] = (nc + i < vend) ? ex2_fast(__uint_as_float(v[i]) * c2 - lse2) : 0.f;
+          }
         } else {
 #pragma unroll
           for (int i = 0; i < 32; ++i) g[i] = 0.f;
