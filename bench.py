@@ -517,6 +517,8 @@ def main():
     if sharded_path:
         import torch.distributed as dist
 
+        # no NVLink multicast objects (NVLS) on shared GPUs: a plain ring all-reduce of dW
+        os.environ.setdefault("NCCL_NVLS_ENABLE", "0")
         if "MASTER_ADDR" not in os.environ:  # one process, not under a launcher
             os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=os.environ.get("MASTER_PORT", "29533"),
                               RANK="0", WORLD_SIZE="1")
