@@ -100,6 +100,14 @@ class ShardedKL:
         self._saved = dict(H=H, W=W, topk_idx=topk_idx, topk_logits=topk_logits, valid=valid, lse=lse, local=local)
         return local
 
+    def state(self):
+        """What the backward of the last forward needs (its inputs, lse and scales), to be
+        handed back with restore() when another forward has run through this object since."""
+        return dict(self._state())
+
+    def restore(self, state):
+        self._saved = dict(state)
+
     def _state(self, need_scale=False):
         if self._saved is None or (need_scale and "grad_scale" not in self._saved):
             raise RuntimeError("ShardedKL: run forward_local and finish (or forward) before this step")
@@ -143,13 +151,13 @@ class _ShardedFn(torch.autograd.Function):
         loss = sharded.forward(H, W, topk_idx, topk_logits, valid)
         # this call's own state: another forward through the same object (a second
         # micro-batch) may come before this call's backward
-        ctx.state = dict(sharded._saved)
+        ctx.state = sharded.state()
         return loss
 
     @staticmethod
     def backward(ctx, grad):
         g = grad.detach().to(torch.float32).reshape(())
-        ctx.sharded._saved = ctx.state
+        ctx.sharded.restore(ctx.state)
         dH, dW = ctx.sharded.backward(1.0, g)
         if ctx.w_dtype != torch.float32:
             dW = dW.to(ctx.w_dtype)
