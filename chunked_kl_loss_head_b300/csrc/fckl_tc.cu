@@ -333,28 +333,31 @@ struct FwdEpi {
       uint32_t v[32];
       tmem_ld_32x32(taddr + c, v);
       tmem_ld_wait();
-      float u[32];
-      float mx = -INFINITY;
+      // the max on the raw logits (c2 > 0 keeps the order), the scale folded into the
+      // exponent's multiply-add
+      float z[32];
+      float mz = -INFINITY;
       if (n0 + c + 32 <= V) {  // a whole chunk of vocabulary columns (all but the last tile's end)
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          u[i] = __uint_as_float(v[i]) * c2;
-          mx = fmaxf(mx, u[i]);
+          z[i] = __uint_as_float(v[i]);
+          mz = fmaxf(mz, z[i]);
         }
       } else {
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          u[i] = (n0 + c + i < V) ? __uint_as_float(v[i]) * c2 : -INFINITY;
-          mx = fmaxf(mx, u[i]);
+          z[i] = (n0 + c + i < V) ? __uint_as_float(v[i]) : -INFINITY;
+          mz = fmaxf(mz, z[i]);
         }
       }
+      const float mx = mz * c2;
       if (mx > m_run) {
         s_run *= ex2_fast(m_run - mx);
         m_run = mx;
       }
       float s = 0.f;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) s += ex2_fast(u[i] - m_run);
+      for (int i = 0; i < 32; ++i) s += ex2_fast(fmaf(z[i], c2, -m_run));
       s_run += s;
       while (nid < n0 + c + 32) {
         zk[row * K + k] = pick32(v, static_cast<int>(nid - (n0 + c)));

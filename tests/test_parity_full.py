@@ -323,8 +323,10 @@ def test_long_context_chunk_sweep():
         assert e_dW <= 1e-3 and e_dH <= 1e-2
         if chunk == 16384:
             # chunks above 4096 rows run their backward in 4096-row blocks: the same
-            # gradient arithmetic as chunks of 4096
-            assert torch.equal(r["dW"], base["dW"]) and torch.equal(r["dH"], base["dH"])
+            # gradient arithmetic as chunks of 4096.  dW is bit for bit equal (each block
+            # writes each element once, in block order); dH's per-stripe reduce-adds may
+            # land in another order from run to run, so dH is compared above within 1e-2.
+            assert torch.equal(r["dW"], base["dW"])
     del runs, base
     # chunk 1024: four chunks of the prefix, 16384-column stripes (13, the last ragged)
     check_prefix(wl, 1024)

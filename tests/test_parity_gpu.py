@@ -95,11 +95,14 @@ def test_chunk_above_the_backward_block(dtype):
     a = run_gpu(x, 6000)
     check(x, a, label=f"{dtype} chunk 6000")
     b = run_gpu(x, 4096)
-    # the backward blocks are the same as chunk 4096's, so the gradients are bit for bit equal
+    # the backward blocks are the same as chunk 4096's.  dW is bit for bit equal: each block
+    # writes each dW element once, in block order.  dH's fp32 accumulator takes one
+    # reduce-add per vocab stripe, and tiles of consecutive stripes overlap in time, so the
+    # order of those adds (dH's last bits) may differ from run to run.
     assert a["loss"] == b["loss"]
     np.testing.assert_array_equal(a["lse"], b["lse"])
     np.testing.assert_array_equal(a["dW"], b["dW"])
-    np.testing.assert_array_equal(a["dH"], b["dH"])
+    assert rel_max(a["dH"], b["dH"]) <= TOL[dtype]["grad"]
 
 
 @pytest.mark.parametrize("chunk", [128, 100, 1000])
@@ -212,6 +215,13 @@ def test_bad_index_reports_status(dtype):
     d = to_device(x)
     ws = api.workspace(100, 32, 400, 4, 64, d["H"].dtype)
     assert api.fckl_get_error(ws) == 0
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_negative_grad_loss(dtype):
+    """A negative gradient of the loss (g = -1.5): the gradient tiles carry the sign."""
+    x = make_small(T=700, d=64, V=5000, K=9, tau=1.1, dtype=dtype, seed=34, mask="random", mask_frac=0.1)
+    check(x, run_gpu(x, 256, grad_loss=-1.5), grad_loss=-1.5, label=f"{dtype} g=-1.5")
 
 
 def test_autograd_module_matches_abi():
