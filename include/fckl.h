@@ -107,6 +107,10 @@ FCKL_API fckl_status fckl_forward(const void* H, const void* W, const int32_t* t
  *   grad_scale device float32 scalar or NULL; when given, g is multiplied by it
  *   dH         device [T, d] in `dtype`, overwritten; rows of ignored tokens are 0
  *   dW         device float32 [V, d], overwritten
+ * Reproducibility: loss, lse and dW are bit for bit the same from run to run.  On the bf16
+ * path dH is accumulated in float32 by one reduce-add per vocab stripe, and tiles of
+ * consecutive stripes run at the same time, so the order of those adds (and the last bits
+ * of dH) can change from run to run.
  * Returns FCKL_OK once the work is queued on `stream`. */
 FCKL_API fckl_status fckl_backward(const void* H, const void* W, const int32_t* topk_idx,
                           const float* topk_logits, const uint8_t* valid, int64_t T, int64_t d,
