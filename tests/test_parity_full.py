@@ -328,5 +328,6 @@ def test_long_context_chunk_sweep():
             # land in another order from run to run, so dH is compared above within 1e-2.
             assert torch.equal(r["dW"], base["dW"])
     del runs, base
-    # chunk 1024: four chunks of the prefix, 16384-column stripes (13, the last ragged)
+    # chunk 1024: four backward blocks of the prefix (the dW read-modify-write across blocks)
+    # over 8192-column stripes (25, the last ragged)
     check_prefix(wl, 1024)

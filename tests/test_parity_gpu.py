@@ -82,9 +82,9 @@ def test_fp32_several_chunks_and_stripes():
 
 
 def test_bf16_several_chunks_and_stripes():
-    # chunk 4096 -> stripes of 4096 vocab columns: 5 stripes, the last ragged (3616 columns),
-    # so all three gradient buffers rotate
-    x = make_small(T=5000, d=64, V=20000, K=13, tau=1.5, dtype="bf16", seed=1, mask="random", mask_frac=0.1)
+    # stripes of 8192 vocab columns: 5 stripes, the last ragged (7232 columns), so the three
+    # gradient buffers rotate; two backward blocks (4096 + 904 rows)
+    x = make_small(T=5000, d=64, V=40000, K=13, tau=1.5, dtype="bf16", seed=1, mask="random", mask_frac=0.1)
     check(x, run_gpu(x, 4096), label="bf16 multi-chunk/stripe")
 
 
