@@ -18,13 +18,14 @@ namespace {
 
 constexpr size_t kAlign = 256;
 // Vocab columns of one stripe of the bf16 backward.  It keeps three gradient stripes
-// G[block, S] bf16 in flight (one being written, two being read), 48 KiB per row of the
-// block: 192 MiB for a block of 4096 rows.  Wider stripes mean fewer passes of the block's
-// fp32 dH accumulator (one reduce per stripe); the gradient buffers do not stay in the
-// 126 MB L2 next to the rest of a block's working set at any width that keeps those passes
-// few.  Measured at the gpt-oss shapes, 8192 columns took 0.8% less time per step than
-// 4096 (the backward 1.3% faster, the forward 0.9% slower under the shared power cap).
-constexpr int64_t kStripeCols = 8192;
+// G[block, S] bf16 in flight (one being written, two being read), 96 KiB per row of the
+// block: 384 MiB for a block of 4096 rows.  Wider stripes mean fewer passes of the block's
+// fp32 dH accumulator (one reduce per stripe, each covering S columns of MMA work); the
+// gradient buffers do not stay in the 126 MB L2 next to the rest of a block's working set
+// at any width that keeps those passes few.  Measured at the gpt-oss shapes (ABAB on one
+// box), 8192 columns took 0.8% less time per step than 4096, and 16384 another 0.9% less
+// than 8192; the peak device memory grows by 0.1 and 0.18 GiB.
+constexpr int64_t kStripeCols = 16384;
 // The f32 path keeps one stripe G[block, S] f32 within this budget.
 constexpr size_t kStripeBudgetBytesF32 = size_t(64) << 20;
 // Rows of one backward block.  The backward works through a chunk in blocks of at most this

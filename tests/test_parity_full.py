@@ -329,5 +329,5 @@ def test_long_context_chunk_sweep():
             assert torch.equal(r["dW"], base["dW"])
     del runs, base
     # chunk 1024: four backward blocks of the prefix (the dW read-modify-write across blocks)
-    # over 8192-column stripes (25, the last ragged)
+    # over 16384-column stripes (13, the last ragged)
     check_prefix(wl, 1024)

@@ -82,9 +82,9 @@ def test_fp32_several_chunks_and_stripes():
 
 
 def test_bf16_several_chunks_and_stripes():
-    # stripes of 8192 vocab columns: 5 stripes, the last ragged (7232 columns), so the three
+    # stripes of 16384 vocab columns: 5 stripes, the last ragged (4464 columns), so the three
     # gradient buffers rotate; two backward blocks (4096 + 904 rows)
-    x = make_small(T=5000, d=64, V=40000, K=13, tau=1.5, dtype="bf16", seed=1, mask="random", mask_frac=0.1)
+    x = make_small(T=5000, d=64, V=70000, K=13, tau=1.5, dtype="bf16", seed=1, mask="random", mask_frac=0.1)
     check(x, run_gpu(x, 4096), label="bf16 multi-chunk/stripe")
 
 
