@@ -290,6 +290,16 @@ def test_bounded_wait_reports_timeout():
     check(x, run_gpu(x, 64), label="after a timeout")
 
 
+@pytest.mark.parametrize("K", [31, 32, 33, 64, 65, 127, 128, 129])
+def test_teacher_prep_k_edges(K):
+    """K at the edges of the teacher-prep kernels: one, two or four sort keys per lane (up
+    to 32, 64, 128 ids) and the ranking kernel above 128; duplicates planted."""
+    x = make_small(T=90, d=32, V=3000, K=K, tau=1.3, dtype="bf16", seed=40 + K, ids="uniform", mask="random",
+                   mask_frac=0.1)
+    x["topk_idx"][7, K - 1] = x["topk_idx"][7, 0]
+    check(x, run_gpu(x, 64), label=f"K={K}")
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_largest_k(dtype):
     x = make_small(T=70, d=64, V=5000, K=1024, tau=1.3, dtype=dtype, seed=32, ids="uniform")
