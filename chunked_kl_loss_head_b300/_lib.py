@@ -24,6 +24,7 @@ PROTOTYPES = {
     "fckl_get_error": (c_i32, [c_vp, c_vp]),
     "fckl_loss_partials": (c_i32, [c_vp, c_sz, c_vp, c_vp]),
     "fckl_loss_finish": (c_i32, [c_vp, c_vp, c_vp, c_vp, c_vp]),
+    "fckl_cast_f32_to_bf16": (c_i32, [c_vp, c_vp, c_i64, c_vp]),
     "fckl_status_string": (ctypes.c_char_p, [c_i32]),
     "fckl_launch_count": (c_i64, []),
     "fckl_profile_enable": (None, [ctypes.c_int]),

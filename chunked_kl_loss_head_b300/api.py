@@ -122,6 +122,25 @@ def fckl_loss_finish(total, local, loss, grad_scale, stream=None):
            "fckl_loss_finish")
 
 
+def fckl_cast_f32_to_bf16(src, dst, stream=None):
+    """dst (bfloat16) = src (float32) rounded to nearest even, element by element."""
+    if src.dtype != torch.float32 or dst.dtype != torch.bfloat16 or src.numel() != dst.numel():
+        raise TypeError("float32 source and bfloat16 destination of the same size expected")
+    _check(lib().fckl_cast_f32_to_bf16(_ptr(src), _ptr(dst), src.numel(), _stream(stream)), "fckl_cast_f32_to_bf16")
+
+
+def to_dtype(dW, dtype, stream=None):
+    """dW in `dtype`: itself when it already has it, the library's cast from float32 to
+    bfloat16 otherwise (any other pair is refused)."""
+    if dW.dtype == dtype:
+        return dW
+    if dW.dtype != torch.float32 or dtype != torch.bfloat16:
+        raise TypeError(f"no cast from {dW.dtype} to {dtype}")
+    out = torch.empty(dW.shape, dtype=dtype, device=dW.device)
+    fckl_cast_f32_to_bf16(dW, out, stream)
+    return out
+
+
 def fckl_topk_extract(logits, K, topk_idx, topk_logits, stream=None):
     """Per row of logits [T, V] (float32 or bfloat16): the K largest values and their ids,
     value descending then id ascending, into topk_idx [T, K] int32 / topk_logits float32."""

@@ -54,10 +54,8 @@ class _FusedChunkedKL(torch.autograd.Function):
         g = grad.detach().to(torch.float32).contiguous()
         dH, dW = api.backward(H, W, topk_idx, topk_logits, valid, lse, ctx.tau, ctx.chunk, grad_loss=1.0,
                               ws=ctx.ws, grad_scale=g)
-        if W.dtype != torch.float32:
-            # dW accumulates in float32 across chunks; the gradient takes W's dtype
-            dW = dW.to(W.dtype)
-        return dH, dW, None, None, None, None, None, None
+        # dW accumulates in float32 across chunks; the gradient takes W's dtype
+        return dH, api.to_dtype(dW, W.dtype), None, None, None, None, None, None
 
 
 def fused_chunked_kl_loss(hidden, lm_head_weight, topk_idx, topk_logits, valid=None, tau=1.0, chunk=4096,

@@ -398,6 +398,16 @@ fckl_status fckl_loss_finish(const double* total, const double* local, float* lo
   return step(FCKL_K_REDUCE, st, [&] { return launch_loss_finish(total, local, loss, grad_scale, st); });
 }
 
+fckl_status fckl_cast_f32_to_bf16(const float* src, void* dst, int64_t n, void* stream) {
+  if (n < 0 || (n > 0 && (!src || !dst))) return FCKL_ERR_INVALID_ARG;
+  if (n % 4 != 0 || !aligned(src, 16) || !aligned(dst, 8)) return FCKL_ERR_UNSUPPORTED;
+  if (n == 0) return FCKL_OK;
+  int num_sms = 0;
+  FCKL_TRY(device_info(&num_sms));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return step(FCKL_K_OTHER, st, [&] { return launch_f32_to_bf16(src, dst, n, st); });
+}
+
 fckl_status fckl_get_error(void* ws, void* stream) {
   if (!ws) return FCKL_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -439,7 +439,7 @@ cudaError_t launch_loss_finish(const double* total, const double* local, float* 
 }
 
 cudaError_t launch_f32_to_bf16(const float* src, void* dst, int64_t n, cudaStream_t st) {
-  const int64_t n4 = n / 4;  // n is a multiple of 8 (d % 8 == 0)
+  const int64_t n4 = n / 4;  // n is a multiple of 4 (d % 8 == 0 for dH; checked for the C-ABI cast)
   const int threads = 256;
   int64_t blocks = (n4 + threads - 1) / threads;
   if (blocks > 148 * 16) blocks = 148 * 16;

@@ -159,9 +159,8 @@ class _ShardedFn(torch.autograd.Function):
         g = grad.detach().to(torch.float32).reshape(())
         ctx.sharded.restore(ctx.state)
         dH, dW = ctx.sharded.backward(1.0, g)
-        if ctx.w_dtype != torch.float32:
-            dW = dW.to(ctx.w_dtype)
-        return dH, dW, None, None, None, None
+        # dW is summed over ranks in float32; the gradient takes W's dtype
+        return dH, api.to_dtype(dW, ctx.w_dtype), None, None, None, None
 
 
 class ShardedFusedChunkedKLLoss(torch.nn.Module):

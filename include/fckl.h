@@ -161,6 +161,13 @@ FCKL_API fckl_status fckl_loss_partials(const void* ws, size_t ws_bytes, double*
 FCKL_API fckl_status fckl_loss_finish(const double* total, const double* local, float* loss, float* grad_scale,
                                       void* stream);
 
+/* dst[i] = src[i] rounded to bfloat16 (to nearest, ties to even), for i < n: for a caller
+ * holding dW in float32 whose weights are bf16 (an autograd gradient takes the weights'
+ * dtype).  The pages have no counterpart: it is the cast at the end of the user's backward.
+ * Needs n % 4 == 0, src 16-byte and dst 8-byte aligned (FCKL_ERR_UNSUPPORTED), n >= 0 and
+ * non-null pointers when n > 0 (FCKL_ERR_INVALID_ARG).  Asynchronous on `stream`. */
+FCKL_API fckl_status fckl_cast_f32_to_bf16(const float* src, void* dst, int64_t n, void* stream);
+
 /* Waits for `stream`, then returns and clears the status word the GPU wrote in
  * the workspace (FCKL_OK, FCKL_ERR_BAD_INDEX or FCKL_ERR_TIMEOUT), or
  * FCKL_ERR_CUDA when the wait or the copy itself failed. */

@@ -122,3 +122,14 @@ def test_data_parallel_calls_reject_bad_arguments():
         assert L.fckl_loss_finish(*args, None) == 1
     assert L.fckl_loss_finish(ctypes.c_void_p((1 << 20) + 4), p, p, p, None) == 1
     assert L.fckl_loss_finish(p, p, ctypes.c_void_p((1 << 20) + 2), p, None) == 1
+
+
+def test_cast_rejects_bad_arguments():
+    L = _lib.lib()
+    p = ctypes.c_void_p(1 << 20)
+    assert L.fckl_cast_f32_to_bf16(None, p, 8, None) == 1
+    assert L.fckl_cast_f32_to_bf16(p, p, -4, None) == 1
+    assert L.fckl_cast_f32_to_bf16(p, p, 6, None) == 2  # not a multiple of 4
+    assert L.fckl_cast_f32_to_bf16(ctypes.c_void_p((1 << 20) + 8), p, 8, None) == 2
+    assert L.fckl_cast_f32_to_bf16(p, ctypes.c_void_p((1 << 20) + 4), 8, None) == 2
+    assert L.fckl_cast_f32_to_bf16(None, None, 0, None) == 0  # nothing to do

@@ -255,6 +255,23 @@ def test_autograd_module_bf16():
     assert rel_max(W.grad.float().cpu().numpy(), ref["dW"]) <= TOL["bf16"]["grad"]
 
 
+def test_cast_matches_round_to_nearest_even():
+    """The library's float32 -> bfloat16 cast against torch's (round to nearest, ties to even),
+    bit for bit, on values that include exact ties, subnormals, infinities and signed zeros
+    (NaNs, which some random tie patterns are, are left out: their payloads may differ)."""
+    g = torch.Generator().manual_seed(5)
+    x = torch.randn(4096, generator=g) * torch.exp2(torch.randint(-130, 40, (4096,), generator=g).float())
+    ties = (torch.randint(0, 1 << 16, (256,), generator=g, dtype=torch.int32) << 16) | 0x8000
+    x[:256] = ties.view(torch.float32)
+    x[256:260] = torch.tensor([float("inf"), -float("inf"), 0.0, -0.0])
+    x = x.cuda()
+    out = torch.empty(4096, dtype=torch.bfloat16, device="cuda")
+    api.fckl_cast_f32_to_bf16(x, out)
+    ref = x.to(torch.bfloat16)
+    finite = torch.isfinite(x) | torch.isinf(x)
+    assert torch.equal(out.view(torch.int16)[finite], ref.view(torch.int16)[finite])
+
+
 def test_autograd_module_two_micro_batches():
     """Two calls of one module instance (different sizes, so its workspace is made anew for
     the second), then one backward of their sum: each call's gradients against the oracle."""
