@@ -508,7 +508,7 @@ def main():
     import torch
 
     from chunked_kl_loss_head_b300 import api
-    from gen import make_inputs
+    from gen import make_inputs, make_W
 
     rank, local_rank, world = dist_env()
     torch.cuda.set_device(local_rank)
@@ -527,8 +527,10 @@ def main():
     chunk = args.chunk or cfg.chunks[0]
     peaks = load_peaks()
 
-    # ---- inputs (one independent batch per rank), resident in HBM
-    x = make_inputs(cfg.with_(seed=cfg.seed + rank))
+    # ---- inputs resident in HBM: each rank its own batch of rows, W the same on every rank
+    # (the lm_head is replicated); rank 0's inputs are the single-GPU workload's
+    x = make_inputs(cfg.with_(seed=cfg.seed + rank), with_W=False)
+    x["W"] = make_W(cfg)
     n_valid = int(x["valid"].sum())
     T, d, V, K = cfg.T, cfg.d, cfg.V, cfg.K
     tdt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
