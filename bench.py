@@ -127,6 +127,27 @@ class ClockSampler:
                     power_w_max=max(pw) if pw else None, samples=len(rows), reasons=reasons)
 
 
+def host_info():
+    """The host the CPU legs run on: CPU model, and the BLAS library numpy calls with the
+    threads it runs (the oracle's matrix products are its only multi-threaded part)."""
+    info = dict(cores=len(os.sched_getaffinity(0)))
+    try:
+        with open("/proc/cpuinfo") as f:
+            info["cpu_model"] = next((ln.split(":", 1)[1].strip() for ln in f if ln.startswith("model name")), None)
+    except OSError:
+        pass
+    try:
+        from threadpoolctl import threadpool_info
+
+        blas = [p for p in threadpool_info() if p.get("user_api") == "blas"]
+        if blas:
+            info["blas"] = f"{blas[0].get('internal_api')} {blas[0].get('version')}"
+            info["cores"] = int(blas[0].get("num_threads") or info["cores"])
+    except ImportError:
+        pass
+    return info
+
+
 def cpu_oracle_rate(cfg, W_bits, rows, reps=1):
     """Oracle fwd+bwd (fp64, full-vocab logit rows, analytic dH / dW) on `rows` rows of
     the workload; returns (tokens/s, seconds)."""
@@ -152,20 +173,21 @@ def run_reference(args, cfg):
     from gen import make_W
 
     W_bits = make_W(cfg)
-    rows = args.ref_rows
-    cores = len(os.sched_getaffinity(0))
+    rows = min(args.ref_rows, cfg.T)
     for _ in range(args.warmup):
         cpu_oracle_rate(cfg, W_bits, rows)
     t = 0.0
     for _ in range(args.steps):
         t += cpu_oracle_rate(cfg, W_bits, rows)[1]
     rate = rows * args.steps / t
+    host = host_info()
     sample = f"oracle fwd+bwd on rows 0..{rows - 1} of {cfg.name} per step (fp64 numpy/BLAS)"
     line = dict(impl="reference", metric=METRIC, value=rate, unit="tokens/s", n_gpus=args.gpus, steps=args.steps,
                 warmup=args.warmup, ms_per_step=1e3 * t / args.steps, higher_is_better=True, scaling="weak",
                 vs_baseline=None, dtype="f64", data="synthetic",
                 config=dict(workload=cfg.name, T=cfg.T, d=cfg.d, V=cfg.V, K=cfg.K, tau=cfg.tau),
-                cpu_baseline=dict(value=rate, unit="tokens/s", cores=cores, kind="oracle", sample=sample),
+                cpu_baseline=dict(value=rate, unit="tokens/s", cores=host["cores"], kind="oracle", sample=sample,
+                                  cpu_model=host.get("cpu_model"), blas=host.get("blas")),
                 e2e=dict(value=rate, unit="tokens/s", h2d_bytes_per_step=0, d2h_bytes_per_step=0))
     print(json.dumps(line), flush=True)
 
@@ -356,8 +378,9 @@ def run_topk(args, cfg):
         t0 = time.perf_counter()
         topk_rows(bf16_bits_to_f32(host[:rows]), K)
         secs = time.perf_counter() - t0
-        cpu = dict(value=rows / secs, unit="rows/s", cores=len(os.sched_getaffinity(0)), kind="oracle",
-                   sample=f"oracle top-K (numpy lexsort per row) on rows 0..{rows - 1}; {secs:.2f} s")
+        # numpy's sort runs on one thread
+        cpu = dict(value=rows / secs, unit="rows/s", cores=1, kind="oracle", cpu_model=host_info().get("cpu_model"),
+                   sample=f"oracle top-K (numpy lexsort per row, one thread) on rows 0..{rows - 1}; {secs:.2f} s")
     # DRAM bytes per launch from the committed ncu capture of this workload, while the kernel
     # source is the one that capture ran
     traffic = None
@@ -709,7 +732,9 @@ def main():
         cpu_rows = min(args.cpu_rows, T)
         rate, secs = cpu_oracle_rate(cfg, h["W"].view(torch.int16).numpy().view(np.uint16)
                                      if tdt == torch.bfloat16 else h["W"].numpy(), cpu_rows)
-        cpu = dict(value=rate, unit="tokens/s", cores=len(os.sched_getaffinity(0)), kind="oracle",
+        host = host_info()
+        cpu = dict(value=rate, unit="tokens/s", cores=host["cores"], kind="oracle",
+                   cpu_model=host.get("cpu_model"), blas=host.get("blas"),
                    sample=f"oracle fwd+bwd (fp64, full-vocab logit rows, analytic dH/dW) on rows 0..{cpu_rows - 1}"
                           f" of {cfg.name}; {secs:.1f} s")
 

@@ -226,6 +226,18 @@ def test_negative_grad_loss(dtype):
     check(x, run_gpu(x, 256, grad_loss=-1.5), grad_loss=-1.5, label=f"{dtype} g=-1.5")
 
 
+@pytest.mark.parametrize("dtype,tau", [("bf16", 0.05), ("bf16", 30.0), ("f32", 0.2), ("f32", 30.0)])
+def test_extreme_temperatures(dtype, tau):
+    """Sharp and flat distributions.  At tau = 0.05 the scaled student logits z/tau reach
+    about 100 (most of a row's exponentials underflow next to its max, so the online max
+    must be right tile by tile) and both softmaxes are near one-hot; at
+    tau = 30 both are near uniform, so q - p is small everywhere and dz is a difference of
+    close numbers.  Teacher logits sit at an offset of 40."""
+    x = make_small(T=700, d=64, V=3000, K=17, tau=tau, dtype=dtype, seed=61, mask="random", mask_frac=0.1,
+                   logit_offset=40.0)
+    check(x, run_gpu(x, 256), label=f"{dtype} tau={tau}")
+
+
 def test_autograd_module_matches_abi():
     from chunked_kl_loss_head_b300 import FusedChunkedKLLoss
 
