@@ -143,7 +143,18 @@ def host_info():
         if blas:
             info["blas"] = f"{blas[0].get('internal_api')} {blas[0].get('version')}"
             info["cores"] = int(blas[0].get("num_threads") or info["cores"])
+            return info
     except ImportError:
+        pass
+    # without threadpoolctl: numpy's build record names the library; OpenBLAS runs one
+    # thread per available core unless OPENBLAS_NUM_THREADS says otherwise
+    try:
+        blas = np.show_config(mode="dicts")["Build Dependencies"]["blas"]
+        info["blas"] = f"{blas.get('name')} {blas.get('version')}"
+        env = os.environ.get("OPENBLAS_NUM_THREADS") or os.environ.get("OMP_NUM_THREADS")
+        if env and env.isdigit() and "openblas" in str(blas.get("name")):
+            info["cores"] = min(info["cores"], int(env))
+    except (KeyError, TypeError, AttributeError):
         pass
     return info
 
