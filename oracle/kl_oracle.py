@@ -29,7 +29,11 @@ s_t = (H_t . W^T) / tau over the full vocabulary:
     dH        = dz . W,     dW = dz^T . H
 
 N = 0 gives loss 0 and zero gradients.  Duplicate ids in a row add up
-termwise.  Everything is fp64; the full logit row of every row is built
+termwise.  A cached logit of -inf is an entry the cache does not hold: its p is
+0 and its KL term is 0 (the divergence sums over the support of p, the usual
+0 log 0 = 0), so it is the same as leaving the entry out; every valid row needs
+at least one finite logit.  Ignored rows contribute nothing whatever their
+teacher logits hold.  Everything is fp64; the full logit row of every row is built
 (row blocks only bound host memory), and the gradients are the analytic
 ones above.
 """
@@ -96,7 +100,10 @@ def fwd_bwd(H, W, topk_idx, topk_logits, valid, tau, grad=1.0, N=None, want_grad
         lse[b0:b1] = lse_b
         rows = np.arange(b1 - b0)[:, None]
         log_q_at = s[rows, idx[b0:b1]] - lse_b[:, None]
-        rl = (p[b0:b1] * (logp[b0:b1] - log_q_at)).sum(axis=1)
+        pb = p[b0:b1]
+        with np.errstate(invalid="ignore"):
+            terms = pb * (logp[b0:b1] - log_q_at)
+        rl = np.where(pb > 0, terms, 0.0).sum(axis=1)  # terms outside the support of p are 0
         row_loss[b0:b1] = np.where(valid[b0:b1], rl, 0.0)
         if not want_grads:
             continue

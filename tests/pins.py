@@ -16,7 +16,9 @@ student softmax, mean over valid rows), through:
 * rows of the logit gradient summing to zero;
 * the closed form at W = 0 (uniform student);
 * the temperature identity, shift / permutation invariance of the teacher,
-  additivity over row subsets and the ignored-row contract.
+  additivity over row subsets and the ignored-row contract;
+* entries of logit -inf being the same as entries left out (KL sums over the
+  support of p).
 """
 
 from __future__ import annotations
@@ -228,6 +230,36 @@ def pin_ignored_rows(f):
     assert np.array_equal(b["dH"][[0, 2, 3, 5]], a["dH"][[0, 2, 3, 5]])
 
 
+def pin_absent_entries(f):
+    """A cached logit of -inf is an entry the cache does not hold: appending (id, -inf)
+    pairs to every row (ids already in the row or not) changes nothing, since the KL
+    divergence sums over the support of p (0 log 0 = 0)."""
+    H, W, idx, lg, valid = _tiny(seed=53, T=6, d=5, V=16, K=4, ignored=(2,))
+    a = f(H=H, W=W, topk_idx=idx, topk_logits=lg, valid=valid, tau=1.3, grad=0.8)
+    extra_idx = np.stack([np.array([(t * 5 + 3) % 16, idx[t, 0]]) for t in range(6)])
+    idx2 = np.concatenate([idx, extra_idx], axis=1)
+    lg2 = np.concatenate([lg, np.full((6, 2), -np.inf)], axis=1)
+    b = f(H=H, W=W, topk_idx=idx2, topk_logits=lg2, valid=valid, tau=1.3, grad=0.8)
+    assert np.isfinite(b["loss"]) and abs(b["loss"] - a["loss"]) <= 1e-13 * abs(a["loss"]), "-inf entries"
+    assert _rel(b["row_loss"], a["row_loss"]) <= 1e-13
+    assert _rel(b["dH"], a["dH"]) <= 1e-13 and _rel(b["dW"], a["dW"]) <= 1e-13
+
+
+def pin_ignored_rows_hold_anything(f):
+    """An ignored row's teacher logits are never used: NaN or infinite values there give
+    the same loss and gradients as finite ones, and its dH row stays exactly 0."""
+    H, W, idx, lg, valid = _tiny(seed=59, T=5, d=4, V=12, K=3, ignored=(0, 3))
+    a = f(H=H, W=W, topk_idx=idx, topk_logits=lg, valid=valid, tau=0.9)
+    lg2 = lg.copy()
+    lg2[0] = np.nan
+    lg2[3] = [np.inf, -np.inf, np.nan]
+    b = f(H=H, W=W, topk_idx=idx, topk_logits=lg2, valid=valid, tau=0.9)
+    assert b["loss"] == a["loss"], "ignored rows' teacher data reach the loss"
+    assert np.array_equal(b["row_loss"], a["row_loss"])
+    assert np.array_equal(b["dH"], a["dH"]) and np.array_equal(b["dW"], a["dW"])
+    assert np.all(b["dH"][[0, 3]] == 0.0)
+
+
 def pin_no_valid_rows(f):
     """N = 0: loss 0 and zero gradients (the reading that avoids 0/0)."""
     H, W, idx, lg, valid = _tiny(seed=37, T=3, d=4, V=8, K=2, ignored=(0, 1, 2))
@@ -247,5 +279,7 @@ ALL_PINS = [
     pin_shift_and_permutation,
     pin_additivity,
     pin_ignored_rows,
+    pin_absent_entries,
+    pin_ignored_rows_hold_anything,
     pin_no_valid_rows,
 ]

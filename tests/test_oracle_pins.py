@@ -63,6 +63,8 @@ MUTATIONS = {
     "student_without_tau": ("s = (H[b0:b1] @ W.T) / tau", "s = (H[b0:b1] @ W.T)"),
     "teacher_scattered_to_wrong_ids": ("idx[b0:b1].ravel()),", "np.roll(idx[b0:b1], 1, axis=1).ravel()),"),
     "transposed_dH": ("dH[b0:b1] = dz @ W", "dH[b0:b1] = (W.T @ dz.T).T[:, ::-1]"),
+    "terms_outside_support_kept": ("rl = np.where(pb > 0, terms, 0.0).sum(axis=1)", "rl = terms.sum(axis=1)"),
+    "ignored_rows_masked_by_product": ("dz[~valid[b0:b1]] = 0.0", "dz *= valid[b0:b1, None]"),
 }
 
 
