@@ -214,7 +214,8 @@ __device__ __forceinline__ void merge_partial(float& m, float& s, float qm, floa
 }
 
 // One warp per row: merge the (max, sum) partials of every 256-wide vocab tile into the
-// row's logsumexp, then loss_t = sum_k p_k (log p_k - s_k + lse_t) with s_k = z_k / tau.
+// row's logsumexp, then loss_t = sum_k p_k (log p_k - s_k + lse_t) with s_k = z_k / tau,
+// over the pairs with p_k > 0 (0 log 0 = 0); ignored rows get loss_t = 0.
 // Partials are in base-2 units (u = z * log2(e) / tau).  Each lane merges its share of the
 // partials as it reads them (two per 16-byte load when the rows start on 16-byte
 // boundaries), then the lanes merge theirs; one pass over the partials.
@@ -254,7 +255,11 @@ __global__ void combine_kernel(const float2* __restrict__ part, int nvt, const f
   const bool ok = valid[row] != 0;
   if (ok) {
     const int64_t b = row * K;
-    for (int k = lane; k < K; k += 32) acc += sp[b + k] * (slogp[b + k] - zk[b + k] / tau + l);
+    for (int k = lane; k < K; k += 32) {
+      // a pair outside the support of p (cached logit -inf: log p = -inf) adds 0, not 0 * inf
+      const float pk = sp[b + k];
+      if (pk > 0.f) acc += pk * (slogp[b + k] - zk[b + k] / tau + l);
+    }
   }
   acc = warp_sum(acc);
   if (lane == 0) {

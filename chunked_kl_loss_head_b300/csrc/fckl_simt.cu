@@ -140,7 +140,8 @@ __global__ void __launch_bounds__(256) simt_bwd_kernel(const float* __restrict__
     const int64_t row = m0 + 4 * w + r;
     if (row >= rows) break;
     const float lse2 = lse[row] * kLog2e;
-    const float a = valid[row] ? alpha : 0.f;
+    const bool on = valid[row] != 0;
+    const float a = on ? alpha : 0.f;
     float g[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) g[j] = (n0 + lane + 32 * j < vend) ? exp2f(acc[r][j] * c2 - lse2) : 0.f;
@@ -158,7 +159,8 @@ __global__ void __launch_bounds__(256) simt_bwd_kernel(const float* __restrict__
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int64_t cl = nl0 + lane + 32 * j;
-      if (cl < S) G[row * S + cl] = static_cast<GT>(g[j] * a);
+      // an ignored row's G is 0 whatever its teacher data hold (NaN * 0 would be NaN)
+      if (cl < S) G[row * S + cl] = static_cast<GT>(on ? g[j] * a : 0.f);
     }
   }
 }

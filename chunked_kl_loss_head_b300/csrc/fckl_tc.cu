@@ -377,8 +377,8 @@ constexpr int kWarpStaging = 2 * 32 * 128;
 constexpr int kEpiStaging = 4 * kWarpStaging;
 
 // Backward logit tile of vocab stripe s (columns [s0, s0 + S) with s0 = s * S):
-// G = (exp(s - lse) - p) * alpha, alpha = g / (tau N) for valid rows and 0 for ignored
-// rows, stored as bf16 into gradient buffer s % 3 (columns [buf * S, buf * S + S) of the
+// G = (exp(s - lse) - p) * alpha, alpha = g / (tau N), for valid rows and exactly 0 for
+// ignored rows, stored as bf16 into gradient buffer s % 3 (columns [buf * S, buf * S + S) of the
 // [rows, ldG] buffer, ldG = 3 * S).  Columns at or past V are written as zeros.
 // Each epilogue warp owns 32 rows; per 64-column chunk it converts two 32-column TMEM
 // loads to bf16, writes the 32 x 64 block (32 rows of 128 bytes, 128-byte swizzle) into
@@ -412,9 +412,15 @@ struct BwdEpi {
     const int32_t* ids = sidx + (live ? row : 0) * K;
     int k = K;
     if (live) {
-      lse2 = lse[row] * kLog2e;
-      a = valid[row] ? ctrl->grad_alpha : 0.f;
-      k = lower_bound_ids(ids, K, n0);
+      if (valid[row]) {
+        lse2 = lse[row] * kLog2e;
+        a = ctrl->grad_alpha;
+        k = lower_bound_ids(ids, K, n0);
+      } else {
+        // ignored row: every exponential is exactly 0 and no p is read, so its G row is 0
+        // whatever its teacher data hold (a NaN there would survive a product with 0)
+        lse2 = INFINITY;
+      }
     }
     int64_t nid = (k < K) ? ids[k] : INT64_MAX;
 #pragma unroll 1

@@ -20,7 +20,14 @@
  *   dH = dz . W,   dW = dz^T . H
  *
  * with g = grad_loss (times *grad_scale when given); N = 0 gives loss 0 and
- * zero gradients.  Duplicate ids in a row add up termwise.
+ * zero gradients.  Duplicate ids in a row add up termwise.  A cached logit of
+ * -inf marks a pair the cache does not hold (a row with fewer than K pairs):
+ * its p is 0 and it adds nothing to loss_t (the sum runs over p_tk > 0, as
+ * 0 log 0 = 0), which is the same as leaving it out.  Every valid row needs at
+ * least one finite logit.  Ignored rows (valid[t] == 0) add nothing to the
+ * loss, their dH rows are exactly 0 and they add nothing to dW whatever their
+ * topk_logits hold (NaN and +-inf included); their ids must still lie in
+ * [0, V).  H and W must be finite.
  *
  * Conventions shared by every call:
  *  - All tensors are row-major and contiguous, on the current CUDA device.

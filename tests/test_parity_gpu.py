@@ -238,6 +238,40 @@ def test_extreme_temperatures(dtype, tau):
     check(x, run_gpu(x, 256), label=f"{dtype} tau={tau}")
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_absent_entries(dtype):
+    """Rows with fewer than K cached pairs, padded with logit -inf: such a pair has p = 0
+    and adds nothing (0 log 0 = 0); the oracle is the definition over p's support."""
+    x = make_small(T=3000, d=64, V=9000, K=13, tau=1.1, dtype=dtype, seed=67, mask="random", mask_frac=0.1)
+    rng = np.random.default_rng(67)
+    rows = rng.choice(3000, 1200, replace=False)
+    for t, n in zip(rows, rng.integers(1, 13, size=1200)):  # keep at least one finite logit
+        x["topk_logits"][t, 13 - n:] = -np.inf
+    got = run_gpu(x, 1024)
+    assert np.isfinite(got["loss"]) and np.all(np.isfinite(got["row_loss"]))
+    check(x, got, label=f"{dtype} -inf padded rows")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_ignored_rows_hold_anything(dtype):
+    """NaN and infinite teacher logits in ignored rows change no output: the same loss,
+    lse, per-row losses and dW bit for bit as with finite ones, and dH within the order
+    of its reduce-adds (its ignored rows exactly 0)."""
+    x = make_small(T=5000, d=64, V=20000, K=9, tau=1.3, dtype=dtype, seed=71, mask="random", mask_frac=0.2)
+    a = run_gpu(x, 4096)
+    ign = ~np.asarray(x["valid"]).astype(bool)
+    junk = np.array([np.nan, np.inf, -np.inf], np.float32)
+    x["topk_logits"][ign] = junk[np.arange(int(ign.sum()) * 9).reshape(-1, 9) % 3]
+    x["topk_logits"][np.nonzero(ign)[0][:5]] = np.nan
+    b = run_gpu(x, 4096)
+    assert b["loss"] == a["loss"]
+    np.testing.assert_array_equal(b["lse"], a["lse"])
+    np.testing.assert_array_equal(b["row_loss"], a["row_loss"])
+    np.testing.assert_array_equal(b["dW"], a["dW"])
+    assert np.all(np.isfinite(b["dH"])) and rel_max(b["dH"], a["dH"]) <= TOL[dtype]["grad"]
+    check(x, b, label=f"{dtype} ignored rows with NaN / inf logits")
+
+
 def test_autograd_module_matches_abi():
     from chunked_kl_loss_head_b300 import FusedChunkedKLLoss
 
