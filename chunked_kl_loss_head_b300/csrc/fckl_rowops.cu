@@ -219,14 +219,32 @@ __device__ __forceinline__ void merge_partial(float& m, float& s, float qm, floa
 // Partials are in base-2 units (u = z * log2(e) / tau).  Each lane merges its share of the
 // partials as it reads them (two per 16-byte load when the rows start on 16-byte
 // boundaries), then the lanes merge theirs; one pass over the partials.
-__global__ void combine_kernel(const float2* __restrict__ part, int nvt, const float* __restrict__ zk,
-                               const float* __restrict__ sp, const float* __restrict__ slogp,
-                               const uint8_t* __restrict__ valid, int64_t rows, int K, float tau,
-                               float* __restrict__ lse, float* __restrict__ row_loss) {
+constexpr int kCombineWarps = 8;
+
+__global__ void __launch_bounds__(kCombineWarps * 32)
+    combine_kernel(const float2* __restrict__ part, int nvt, const float* __restrict__ zk,
+                   const float* __restrict__ sp, const float* __restrict__ slogp, const uint8_t* __restrict__ valid,
+                   int64_t rows, int K, float tau, float* __restrict__ lse, float* __restrict__ row_loss) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + warp;
   if (row >= rows) return;
   const float2* pr = part + row * nvt;
+  const bool ok = valid[row] != 0;
+  const int64_t b = row * K;
+  // the row's first 32 * kPre (p, log p, z) triples are loaded before the partials, so
+  // their latency hides under the merge
+  constexpr int kPre = 4;
+  float pp[kPre], lq[kPre], zz[kPre];
+#pragma unroll
+  for (int i = 0; i < kPre; ++i) {
+    const int k = lane + 32 * i;
+    pp[i] = lq[i] = zz[i] = 0.f;
+    if (ok && k < K) {
+      pp[i] = sp[b + k];
+      lq[i] = slogp[b + k];
+      zz[i] = zk[b + k];
+    }
+  }
   float m = -INFINITY, s = 0.f;
   if ((nvt & 1) == 0 && (reinterpret_cast<uintptr_t>(part) & 15) == 0) {
     const float4* p4 = reinterpret_cast<const float4*>(pr);
@@ -251,14 +269,18 @@ __global__ void combine_kernel(const float2* __restrict__ part, int nvt, const f
     m = mm;
   }
   const float l = (m + log2f(s)) * kLn2;
+  // a pair outside the support of p (cached logit -inf: log p = -inf) adds 0, not 0 * inf
   float acc = 0.f;
-  const bool ok = valid[row] != 0;
   if (ok) {
-    const int64_t b = row * K;
-    for (int k = lane; k < K; k += 32) {
-      // a pair outside the support of p (cached logit -inf: log p = -inf) adds 0, not 0 * inf
+#pragma unroll
+    for (int i = 0; i < kPre; ++i) {
+      const float t = pp[i] * (lq[i] - zz[i] / tau + l);
+      acc += (pp[i] > 0.f) ? t : 0.f;
+    }
+    for (int k = lane + 32 * kPre; k < K; k += 32) {
       const float pk = sp[b + k];
-      if (pk > 0.f) acc += pk * (slogp[b + k] - zk[b + k] / tau + l);
+      const float t = pk * (slogp[b + k] - zk[b + k] / tau + l);
+      acc += (pk > 0.f) ? t : 0.f;
     }
   }
   acc = warp_sum(acc);
@@ -414,9 +436,8 @@ cudaError_t launch_prep(const int32_t* idx, const float* logits, int64_t rows, i
 cudaError_t launch_combine(const float2* part, int nvt, const float* zk, const float* sp, const float* slogp,
                            const uint8_t* valid, int64_t rows, int32_t K, float tau, float* lse,
                            float* row_loss, cudaStream_t st) {
-  constexpr int warps = 8;
-  const unsigned grid = static_cast<unsigned>((rows + warps - 1) / warps);
-  combine_kernel<<<grid, warps * 32, 0, st>>>(part, nvt, zk, sp, slogp, valid, rows, K, tau, lse, row_loss);
+  const unsigned grid = static_cast<unsigned>((rows + kCombineWarps - 1) / kCombineWarps);
+  combine_kernel<<<grid, kCombineWarps * 32, 0, st>>>(part, nvt, zk, sp, slogp, valid, rows, K, tau, lse, row_loss);
   return cudaGetLastError();
 }
 
