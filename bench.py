@@ -159,6 +159,17 @@ def host_info():
     return info
 
 
+def rank_inputs(cfg, rank):
+    """One rank's inputs for the token-sharded step: its own batch of rows (the workload's
+    seed + rank) and the same W on every rank (the lm_head is replicated).  Rank 0's
+    inputs are the single-GPU workload's."""
+    from gen import make_inputs, make_W
+
+    x = make_inputs(cfg.with_(seed=cfg.seed + rank), with_W=False)
+    x["W"] = make_W(cfg)
+    return x
+
+
 def cpu_oracle_rate(cfg, W_bits, rows, reps=1):
     """Oracle fwd+bwd (fp64, full-vocab logit rows, analytic dH / dW) on `rows` rows of
     the workload; returns (tokens/s, seconds)."""
@@ -542,8 +553,6 @@ def main():
     import torch
 
     from chunked_kl_loss_head_b300 import api
-    from gen import make_inputs, make_W
-
     rank, local_rank, world = dist_env()
     torch.cuda.set_device(local_rank)
     dist = None
@@ -561,10 +570,8 @@ def main():
     chunk = args.chunk or cfg.chunks[0]
     peaks = load_peaks()
 
-    # ---- inputs resident in HBM: each rank its own batch of rows, W the same on every rank
-    # (the lm_head is replicated); rank 0's inputs are the single-GPU workload's
-    x = make_inputs(cfg.with_(seed=cfg.seed + rank), with_W=False)
-    x["W"] = make_W(cfg)
+    # ---- inputs, resident in HBM
+    x = rank_inputs(cfg, rank)
     n_valid = int(x["valid"].sum())
     T, d, V, K = cfg.T, cfg.d, cfg.V, cfg.K
     tdt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32

@@ -3,8 +3,9 @@
 Under torchrun every rank of the benchmark runs T tokens of its own (weak scaling), and
 the job's time is the slowest rank's.  These tests run that host logic (the max over
 ranks and the whole-job rate) with two gloo ranks, and launch the reference arm under
-torchrun with two processes (rank 0 alone works and prints one line).  The token-sharded
-loss itself, with its all-reduces, is covered by test_dist_sharded_cpu.py."""
+torchrun with two processes (rank 0 alone works and prints one line), and check that the
+ranks' inputs share W and differ in their rows.  The token-sharded loss itself, with its
+all-reduces, is covered by test_dist_sharded_cpu.py."""
 
 import json
 import os
@@ -72,3 +73,21 @@ def test_reference_arm_under_torchrun_prints_one_line():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_ranks_share_W_and_own_their_rows():
+    """Each rank of the benchmark's token-sharded step holds the same lm_head W and its own
+    rows; rank 0's inputs are the single-GPU workload's."""
+    import numpy as np
+
+    sys.path.insert(0, ROOT)
+    import bench
+    from gen import CONFIGS, make_inputs
+
+    cfg = CONFIGS["tiny_fp32"]
+    r0, r1 = bench.rank_inputs(cfg, 0), bench.rank_inputs(cfg, 1)
+    one = make_inputs(cfg)
+    assert np.array_equal(r0["W"], r1["W"])
+    assert not np.array_equal(r0["H"], r1["H"]) and not np.array_equal(r0["topk_idx"], r1["topk_idx"])
+    for k in ("H", "W", "topk_idx", "topk_logits", "valid"):
+        assert np.array_equal(r0[k], one[k]), k
