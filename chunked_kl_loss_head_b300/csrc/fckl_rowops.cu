@@ -217,8 +217,9 @@ __device__ __forceinline__ void merge_partial(float& m, float& s, float qm, floa
 // row's logsumexp, then loss_t = sum_k p_k (log p_k - s_k + lse_t) with s_k = z_k / tau,
 // over the pairs with p_k > 0 (0 log 0 = 0); ignored rows get loss_t = 0.
 // Partials are in base-2 units (u = z * log2(e) / tau).  Each lane merges its share of the
-// partials as it reads them (two per 16-byte load when the rows start on 16-byte
-// boundaries), then the lanes merge theirs; one pass over the partials.
+// partials in one pass: when the rows start on 16-byte boundaries, two partials per 16-byte
+// load and eight loads in flight per batch (the batch's max first, then its exponentials);
+// otherwise one at a time.  Then the lanes merge theirs.
 constexpr int kCombineWarps = 8;
 
 __global__ void __launch_bounds__(kCombineWarps * 32)
@@ -247,13 +248,26 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
   }
   float m = -INFINITY, s = 0.f;
   if ((nvt & 1) == 0 && (reinterpret_cast<uintptr_t>(part) & 15) == 0) {
+    // batches of kBatch 16-byte loads per lane, all issued before any is used; a batch
+    // moves the lane's max once, then adds its partials without branches
     const float4* p4 = reinterpret_cast<const float4*>(pr);
     const int n4 = nvt >> 1;
-#pragma unroll 4
-    for (int j = lane; j < n4; j += 32) {
-      const float4 v = p4[j];
-      merge_partial(m, s, v.x, v.y);
-      merge_partial(m, s, v.z, v.w);
+    constexpr int kBatch = 8;
+    for (int j0 = lane; j0 < n4; j0 += 32 * kBatch) {
+      float4 v[kBatch];
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) {
+        const int j = j0 + 32 * i;
+        v[i] = (j < n4) ? p4[j] : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
+      }
+      float bm = m;
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) bm = fmaxf(bm, fmaxf(v[i].x, v[i].z));
+      if (bm == -INFINITY) continue;  // nothing but empty partials so far
+      s *= exp2f(m - bm);             // m = -inf at the start: s is 0 and stays 0
+      m = bm;
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) s += v[i].y * exp2f(v[i].x - m) + v[i].w * exp2f(v[i].z - m);
     }
   } else {
     for (int j = lane; j < nvt; j += 32) {
